@@ -1,0 +1,435 @@
+"""Benchmark of the SVDQ W4A4 NVFP4 linear (and the AWQ W4A16 modulation GEMV)
+on B300.
+
+One step = one pass of the per-forward hot path of the SVDQ linear over one
+batch: svdq_quantize_act (smoothing, rank-r down projection, e2m1/e4m3
+quantization) then svdq_gemm_w4a4 (tcgen05 NVFP4 product + rank-r up
+projection + bias), on the attention out-projection workload of a 1024x1024
+diffusion transformer: M = 4096 tokens, K = N = 3072, rank 32, synthetic
+outlier-heavy activations.  Weights are packed once, offline, by
+svdq_pack_weights (not timed).  Inputs rotate over enough buffer sets that
+every step reads from HBM, not L2.
+
+The AWQ phase times the 57 stacked adaLN modulation GEMVs (K = 3072,
+N = 6 x 3072, M in {1, 2, 4}) back to back.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "SVDQ W4A4 NVFP4 linear TFLOP/s & % FP4 tensor peak; AWQ W4A16 HBM GB/s"
+L2_BYTES = 126 * 1024 * 1024
+FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- dist
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def time_oracle(case, sample_rows: int, steps: int):
+    """The CPU oracle on `sample_rows` rows of the workload per step (its own
+    packing is offline, not timed).  Returns (seconds per step, flop per step,
+    threads)."""
+    from oracle import svdq
+    X = workloads.make_activations(case, M=sample_rows)
+    W, b = workloads.make_weights(case)
+    xm = svdq.calib_absmax(workloads.make_activations(case))
+    packed = svdq.pack_weights(W, xm, case.rank)
+    svdq.linear_forward(X, packed, b)  # warm-up
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        svdq.linear_forward(X, packed, b)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts), 2.0 * sample_rows * case.N * case.K, os.cpu_count()
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, world, rank, local):
+    import torch
+    import bit_w4a4_diffusion_quantize_b300 as lib
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    case = workloads.CASES[args.workload]
+    M, K, N, r = case.M, case.K, case.N, case.rank
+
+    # ---- inputs and offline packing (not timed)
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    Xbits = workloads.bf16_bits_of(X)
+    xm = lib.svdq_calib_absmax(Xbits)
+    t0 = time.perf_counter()
+    packed = lib.svdq_pack_weights(W, xm, r)
+    pack_s = time.perf_counter() - t0
+
+    def dbits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    set_bytes = (M * K * 2 + M * K // 2 + lib.scale_bytes(M, K) + M * r * 2 + M * N * 2 +
+                 N * K // 2 + lib.scale_bytes(N, K) + r * (N + K) * 2 + N * 2 + K * 4)
+    nsets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    sets = []
+    for _ in range(nsets):
+        s = {
+            "X": dbits(Xbits).view(torch.bfloat16).view(M, K),
+            "inv": torch.from_numpy(packed["inv_lambda"]).to(dev),
+            "L1s": dbits(packed["L1s"]).view(torch.bfloat16),
+            "L2": dbits(packed["L2"]).view(torch.bfloat16),
+            "wc": torch.from_numpy(packed["w_codes"]).to(dev),
+            "ws": torch.from_numpy(packed["w_scales"]).to(dev),
+            "bias": dbits(workloads.bf16_bits_of(b)).view(torch.bfloat16),
+            "ac": torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+            "as": torch.empty(lib.scale_bytes(M, K), dtype=torch.uint8, device=dev),
+            "lora": torch.empty((M, r), dtype=torch.bfloat16, device=dev),
+            "Y": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+        }
+        sets.append(s)
+    sT = packed["w_tensor_scale"]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        s = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        lib.svdq_quantize_act(s["X"], s["inv"], s["L1s"], r, s["ac"], s["as"], s["lora"],
+                              dev_status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        lib.svdq_gemm_w4a4(s["ac"], s["as"], s["wc"], s["ws"], sT, s["lora"], s["L2"],
+                           s["bias"], M, N, K, r, Y=s["Y"], dev_status=status, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            step(i, evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the timed region")
+    t_q = [evs[i][0].elapsed_time(evs[i][1]) * 1e-3 for i in range(args.steps)]
+    t_g = [evs[i][1].elapsed_time(evs[i][2]) * 1e-3 for i in range(args.steps)]
+    t_total = evs[0][0].elapsed_time(evs[-1][2]) * 1e-3
+    t_total = max_over_ranks(t_total, world, dev)
+    flop = 2.0 * M * N * K
+    value = world * args.steps * flop / t_total / 1e12
+
+    # ---- end to end: host (pinned) X in, host Y out, through the layer API
+    layer = lib.SVDQLinear(packed | {"N": N, "K": K, "rank": r}, workloads.bf16_bits_of(b), dev)
+    Xh = torch.from_numpy(Xbits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    Yd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    bufs = (sets[0]["ac"], sets[0]["as"], sets[0]["lora"])
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        layer.forward(Xd, out=Yd, act_buffers=bufs, stream=stream)
+        Yh.copy_(Yd, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world, dev)
+    e2e = {"value": world * args.steps * flop / t_e2e / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+           "ms_per_step": t_e2e / args.steps * 1e3}
+
+    # ---- AWQ W4A16: the stacked modulation GEMVs
+    awq = None
+    if args.awq_blocks > 0:
+        awq = run_awq(args, lib, dev, stream, world)
+
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    g_avg = statistics.mean(t_g)
+    q_avg = statistics.mean(t_q)
+    gemm_tflops = flop / g_avg / 1e12
+    q_bytes = M * K * 2 + M * K // 2 + M * K // 16 + M * r * 2
+    g_bytes = (M * K // 2 + M * K // 16 + N * K // 2 + N * K // 16 + M * r * 2 + r * N * 2 +
+               N * 2 + M * N * 2)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_total / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4",
+        "data": "synthetic (seeded; DiT attention out-projection shapes and outlier statistics)",
+        "config": {"workload": f"{case.name}: SVDQ W4A4 linear M={M} K={K} N={N} rank={r}",
+                   "M": M, "K": K, "N": N, "rank": r,
+                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * set_bytes / 2**20:.0f}"
+                         " MiB > 3x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "tensor", "kernel": "svdq_gemm_w4a4",
+            "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+            "frac": round(gemm_tflops / fp4_peak, 4),
+            "peak_source": f"{pk['source']} bf16 {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
+                           "(nominal fp4/bf16 dense ratio)",
+            "traffic": None,
+            "algorithmic_bytes": g_bytes,
+            "achieved_hbm_gbs": round(g_bytes / g_avg / 1e9, 1),
+        },
+        "kernels": {
+            "svdq_quantize_act": {"us": round(q_avg * 1e6, 2), "bound": "hbm",
+                                  "achieved_gbs": round(q_bytes / q_avg / 1e9, 1),
+                                  "peak_gbs": pk["hbm_gbs"],
+                                  "frac": round(q_bytes / q_avg / 1e9 / pk["hbm_gbs"], 4),
+                                  "algorithmic_bytes": q_bytes},
+            "svdq_gemm_w4a4": {"us": round(g_avg * 1e6, 2), "tflops": round(gemm_tflops, 1)},
+        },
+        "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in e2e.items()},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "pack_seconds": round(pack_s, 2),
+        "wall_s_timed": round(wall, 4),
+    }
+    if awq is not None:
+        line["awq"] = awq
+        line["gpu_launches"] += awq["launches"]
+    return line
+
+
+def run_awq(args, lib, dev, stream, world):
+    import torch
+    pk = peaks()
+    blocks = []
+    for blk in range(args.awq_blocks):
+        W, b = workloads.make_awq_weights(blk)
+        q, s, z = lib.awq_pack_weights(W)
+        blocks.append((torch.from_numpy(q).to(dev),
+                       torch.from_numpy(s.view(np.int16)).to(dev).view(torch.float16),
+                       torch.from_numpy(z.view(np.int16)).to(dev).view(torch.float16),
+                       torch.from_numpy(workloads.bf16_bits_of(b).view(np.int16)).to(dev).view(
+                           torch.bfloat16)))
+    N, K = workloads.AWQ_N, workloads.AWQ_K
+    res = {"metric": "AWQ W4A16 HBM GB/s", "blocks": args.awq_blocks, "K": K, "N": N,
+           "by_M": {}, "launches": 0}
+    for M in (1, 2, 4):
+        X = torch.from_numpy(workloads.bf16_bits_of(workloads.make_awq_activations(M)).view(
+            np.int16)).to(dev).view(torch.bfloat16)
+        Y = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in blocks]
+        for i, (q, s, z, b) in enumerate(blocks):
+            lib.awq_gemv_w4a16(X, q, s, z, b, Y=Y[i], stream=stream)
+        torch.cuda.synchronize()
+        reps = max(1, args.steps // 4)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            for i, (q, s, z, b) in enumerate(blocks):
+                lib.awq_gemv_w4a16(X, q, s, z, b, Y=Y[i], stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / reps
+        t = max_over_ranks(t, world, dev)
+        nbytes = len(blocks) * (N * K // 2 + 4 * N * (K // 64) + M * K * 2 + M * N * 2 + N * 2)
+        gbs = nbytes / t / 1e9
+        res["by_M"][str(M)] = {"us_per_stack": round(t * 1e6, 1), "gbs": round(world * gbs, 1),
+                               "frac": round(gbs / pk["hbm_gbs"], 4)}
+        res["launches"] += reps * len(blocks)
+    res["roofline"] = {"bound": "hbm", "kernel": "awq_gemv_w4a16",
+                       "achieved": res["by_M"]["1"]["gbs"] / world, "peak": pk["hbm_gbs"],
+                       "unit": "GB/s", "frac": res["by_M"]["1"]["frac"], "traffic": None}
+    return res
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    case = workloads.CASES[args.workload]
+    rows = args.oracle_rows
+    t, flop, cores = time_oracle(case, rows, args.steps)
+    value = flop / t / 1e12
+    sample = (f"{rows} of {case.M} rows of the {case.name} workload per step "
+              f"(K={case.K}, N={case.N}, rank {case.rank}); oracle packing not timed")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{case.name}: SVDQ W4A4 linear M={case.M} K={case.K} "
+                               f"N={case.N} rank={case.rank}", "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="attn_out", choices=sorted(workloads.CASES))
+    ap.add_argument("--awq-blocks", type=int, default=workloads.AWQ_BLOCKS)
+    ap.add_argument("--oracle-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return 0
+
+    line = run_gpu(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            case = workloads.CASES[args.workload]
+            t, flop, cores = time_oracle(case, args.oracle_rows, 3)
+            line["cpu_baseline"] = {
+                "value": round(flop / t / 1e12, 5), "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{args.oracle_rows} of {case.M} rows per step, median of 3 "
+                          "(oracle packing not timed)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

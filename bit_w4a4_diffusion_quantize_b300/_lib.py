@@ -1,0 +1,215 @@
+"""ctypes binding of libsvdq (include/svdq.h): argument marshalling only.
+
+Device calls take torch CUDA tensors (PyTorch provides device memory and
+streams); host calls take NumPy arrays.  Outputs that are not passed in are
+allocated here with torch/NumPy; every computation happens in the library.
+A missing library raises ImportError: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsvdq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with "
+        "`python -m bit_w4a4_diffusion_quantize_b300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_c_p = ctypes.c_void_p
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+
+STATUS = {
+    0: "SVDQ_OK", -1: "SVDQ_ERR_NULL", -2: "SVDQ_ERR_SHAPE", -3: "SVDQ_ERR_ALIGN",
+    -4: "SVDQ_ERR_UNSUPPORTED_ARCH", -5: "SVDQ_ERR_CUDA", -6: "SVDQ_ERR_RANK",
+    -7: "SVDQ_ERR_VALUE", -8: "SVDQ_ERR_NOMEM",
+}
+DEV_OK = 0
+DEV_TIMEOUT = 1
+
+_SIGS = {
+    "svdq_status_string": (ctypes.c_char_p, [_i32]),
+    "svdq_check_device": (_i32, []),
+    "svdq_calib_absmax": (_i32, [_c_p, _i64, _i64, _c_p]),
+    "svdq_pack_weights": (_i32, [_c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                 _c_p]),
+    "awq_pack_weights": (_i32, [_c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p]),
+    "svdq_quantize_act": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p,
+                                 _c_p]),
+    "svdq_gemm_w4a4": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _i32,
+                              _i32, _i32, _i32, _c_p, _c_p]),
+    "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
+                              _c_p, _c_p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class SvdqError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        msg = _lib.svdq_status_string(status)
+        super().__init__(f"{call}: {msg.decode() if msg else STATUS.get(status, status)}")
+
+
+def _check(status: int, call: str):
+    if status != 0:
+        raise SvdqError(status, call)
+
+
+def status_name(status: int) -> str:
+    return STATUS.get(status, str(status))
+
+
+def raw_lib():
+    """The ctypes handle (for tests that call the C ABI directly)."""
+    return _lib
+
+
+# --------------------------------------------------------------------------- sizes
+def code_bytes(rows: int, K: int) -> int:
+    return rows * K // 2
+
+
+def scale_bytes(rows: int, K: int) -> int:
+    return ((rows + 127) // 128) * 128 * (K // 16)
+
+
+# --------------------------------------------------------------------------- host calls
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def check_device() -> int:
+    """Status of svdq_check_device (0 when the current device is CC 10.3)."""
+    return int(_lib.svdq_check_device())
+
+
+def svdq_calib_absmax(X_bf16_bits: np.ndarray) -> np.ndarray:
+    X = np.ascontiguousarray(X_bf16_bits, dtype=np.uint16)
+    M, K = X.shape
+    out = np.zeros(K, dtype=np.float32)
+    _check(_lib.svdq_calib_absmax(_np_ptr(X), M, K, _np_ptr(out)), "svdq_calib_absmax")
+    return out
+
+
+def svdq_pack_weights(W: np.ndarray, x_absmax: np.ndarray, rank: int) -> dict:
+    """Offline packing of an nn.Linear weight W [N, K] (float32).  Returns the
+    device-side buffers as NumPy arrays."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    xm = np.ascontiguousarray(x_absmax, dtype=np.float32)
+    N, K = W.shape
+    r = max(int(rank), 0)
+    inv = np.zeros(K, dtype=np.float32)
+    L1s = np.zeros((r, K), dtype=np.uint16)
+    L2 = np.zeros((r, N), dtype=np.uint16)
+    codes = np.zeros((N, K // 2), dtype=np.uint8)
+    scales = np.zeros(scale_bytes(N, K), dtype=np.uint8)
+    sT = np.zeros(1, dtype=np.float32)
+    st = _lib.svdq_pack_weights(_np_ptr(W), N, K, _np_ptr(xm), int(rank), _np_ptr(inv),
+                                _np_ptr(L1s), _np_ptr(L2), _np_ptr(codes), _np_ptr(scales),
+                                _np_ptr(sT))
+    _check(st, "svdq_pack_weights")
+    return {"N": N, "K": K, "rank": int(rank), "inv_lambda": inv, "L1s": L1s, "L2": L2,
+            "w_codes": codes, "w_scales": scales, "w_tensor_scale": float(sT[0])}
+
+
+def awq_pack_weights(W: np.ndarray, group_size: int = 64):
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    G = K // 64 if group_size == 64 and K % 64 == 0 else 1
+    q = np.zeros((N, K // 2), dtype=np.uint8)
+    s = np.zeros((N, G), dtype=np.uint16)
+    z = np.zeros((N, G), dtype=np.uint16)
+    _check(_lib.awq_pack_weights(_np_ptr(W), N, K, int(group_size), _np_ptr(q), _np_ptr(s),
+                                 _np_ptr(z)), "awq_pack_weights")
+    return q, s, z
+
+
+# --------------------------------------------------------------------------- device calls
+def _torch():
+    import torch
+    return torch
+
+
+def _dptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_cuda(t, name):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None,
+                      lora_act=None, dev_status=None, stream=None):
+    """X: CUDA bf16 (or int16/uint16 bits) [M, K]; inv_lambda fp32 [K];
+    L1s bf16 bits [rank, K].  Returns (a_codes, a_scales, lora_act)."""
+    torch = _torch()
+    for t, n in ((X, "X"), (inv_lambda, "inv_lambda"), (L1s, "L1s")):
+        _check_cuda(t, n)
+    M, K = X.shape
+    dev = X.device
+    if a_codes is None:
+        a_codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    if a_scales is None:
+        a_scales = torch.empty(scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    if lora_act is None:
+        lora_act = torch.empty((M, rank), dtype=torch.bfloat16, device=dev)
+    st = _lib.svdq_quantize_act(_dptr(X), _dptr(inv_lambda), _dptr(L1s), M, K, int(rank),
+                                _dptr(a_codes), _dptr(a_scales), _dptr(lora_act),
+                                _dptr(dev_status), _stream_ptr(stream))
+    _check(st, "svdq_quantize_act")
+    return a_codes, a_scales, lora_act
+
+
+def svdq_gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act, L2,
+                   bias, M: int, N: int, K: int, rank: int, Y=None, dev_status=None,
+                   stream=None):
+    """Returns Y [M, N] bf16 (CUDA)."""
+    torch = _torch()
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2, "L2"), (bias, "bias")):
+        _check_cuda(t, n)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    st = _lib.svdq_gemm_w4a4(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales),
+                             float(w_tensor_scale), _dptr(lora_act), _dptr(L2), _dptr(bias),
+                             _dptr(Y), int(M), int(N), int(K), int(rank), _dptr(dev_status),
+                             _stream_ptr(stream))
+    _check(st, "svdq_gemm_w4a4")
+    return Y
+
+
+def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None,
+                   dev_status=None, stream=None):
+    """X: CUDA bf16 [M, K] (M <= 8); returns Y [M, N] bf16."""
+    torch = _torch()
+    for t, n in ((X, "X"), (qweight, "qweight"), (scales, "scales"), (zeros, "zeros"),
+                 (bias, "bias")):
+        _check_cuda(t, n)
+    M, K = X.shape
+    N = qweight.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    st = _lib.awq_gemv_w4a16(_dptr(X), _dptr(qweight), _dptr(scales), _dptr(zeros), _dptr(bias),
+                             _dptr(Y), int(M), int(N), int(K), int(group_size),
+                             _dptr(dev_status), _stream_ptr(stream))
+    _check(st, "awq_gemv_w4a16")
+    return Y

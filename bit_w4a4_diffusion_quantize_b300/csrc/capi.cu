@@ -1,0 +1,206 @@
+// C ABI of libsvdq, device side: argument validation, the compute-capability
+// check (dothoosh.com, "How Nunchaku Lite halves the VRAM of diffusion
+// models", hardware list: the loader validates the CUDA capability and fails
+// with a clear error instead of producing wrong output), TMA descriptor
+// encoding and kernel launches.  Every error is detected before anything is
+// launched.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/svdq.h"
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 supported, 2 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Compute capability required by the sm_103a kernels.
+constexpr int kMajor = 10, kMinor = 3;
+
+svdq_status current_device(int* dev_out, int* num_sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SVDQ_ERR_CUDA;
+  }
+  // test hook: pretend the device has another compute capability ("MAJOR.MINOR")
+  const char* fake = std::getenv("SVDQ_FAKE_COMPUTE_CAPABILITY");
+  if (fake && *fake) {
+    int ma = 0, mi = 0;
+    if (std::sscanf(fake, "%d.%d", &ma, &mi) >= 1 && (ma != kMajor || mi != kMinor))
+      return SVDQ_ERR_UNSUPPORTED_ARCH;
+  }
+  DeviceInfo& d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    int ma = 0, mi = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SVDQ_ERR_CUDA;
+    }
+    d.num_sms = sms;
+    st = (ma == kMajor && mi == kMinor) ? 1 : 2;
+    d.state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return SVDQ_ERR_UNSUPPORTED_ARCH;
+  if (dev_out) *dev_out = dev;
+  if (num_sms) *num_sms = d.num_sms;
+  return SVDQ_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool rank_ok(int r) { return r == 16 || r == 32 || r == 64; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the
+// library links the CUDA runtime statically and never links libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [rows][K/2] bytes of 4-bit codes; box = 128 bytes x box_rows, 128B swizzle
+bool encode_codes(CUtensorMap* map, const uint8_t* ptr, int rows, int K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* svdq_status_string(svdq_status s) {
+  switch (s) {
+    case SVDQ_OK: return "SVDQ_OK";
+    case SVDQ_ERR_NULL: return "SVDQ_ERR_NULL: a required pointer is NULL";
+    case SVDQ_ERR_SHAPE: return "SVDQ_ERR_SHAPE: a size violates the call's shape rules";
+    case SVDQ_ERR_ALIGN: return "SVDQ_ERR_ALIGN: a device pointer is not 16-byte aligned";
+    case SVDQ_ERR_UNSUPPORTED_ARCH:
+      return "SVDQ_ERR_UNSUPPORTED_ARCH: the NVFP4 kernels need a compute capability 10.3 "
+             "(B300) device";
+    case SVDQ_ERR_CUDA: return "SVDQ_ERR_CUDA: a CUDA call failed";
+    case SVDQ_ERR_RANK: return "SVDQ_ERR_RANK: rank not allowed for this call";
+    case SVDQ_ERR_VALUE: return "SVDQ_ERR_VALUE: a value argument is out of its domain";
+    case SVDQ_ERR_NOMEM: return "SVDQ_ERR_NOMEM: host allocation failed";
+  }
+  return "unknown svdq_status";
+}
+
+svdq_status svdq_check_device(void) { return current_device(nullptr, nullptr); }
+
+svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
+                              const uint16_t* L1s, int M, int K, int rank, uint8_t* a_codes,
+                              uint8_t* a_scales, uint16_t* lora_act, int* dev_status,
+                              void* stream) {
+  if (M < 0 || K <= 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  if (M == 0) return SVDQ_OK;
+  if (!X_bf16 || !inv_lambda || !L1s || !a_codes || !a_scales || !lora_act) return SVDQ_ERR_NULL;
+  if (!aligned16(X_bf16) || !aligned16(inv_lambda) || !aligned16(L1s) || !aligned16(a_codes) ||
+      !aligned16(a_scales) || !aligned16(lora_act))
+    return SVDQ_ERR_ALIGN;
+  int sms = 0;
+  svdq_status st = current_device(nullptr, &sms);
+  if (st != SVDQ_OK) return st;
+  cudaError_t e = svdq::launch_quantize_act(X_bf16, inv_lambda, L1s, M, K, rank, a_codes,
+                                            a_scales, lora_act, dev_status,
+                                            static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
+svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
+                           const uint8_t* w_codes, const uint8_t* w_scales,
+                           float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2,
+                           const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
+                           int* dev_status, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  {
+    // a finite power of two in [2^-100, 2^100]
+    int ex = 0;
+    const float m = std::frexp(w_tensor_scale, &ex);
+    if (!std::isfinite(w_tensor_scale) || m != 0.5f || ex - 1 < -100 || ex - 1 > 100)
+      return SVDQ_ERR_VALUE;
+  }
+  if (M == 0) return SVDQ_OK;
+  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2 || !Y)
+    return SVDQ_ERR_NULL;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
+      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2) || !aligned16(Y) ||
+      (bias && !aligned16(bias)))
+    return SVDQ_ERR_ALIGN;
+  svdq_status st = current_device(nullptr, nullptr);
+  if (st != SVDQ_OK) return st;
+  const int block_n = (N % 256 == 0) ? 256 : 128;
+  svdq::GemmMaps maps;
+  if (!encode_codes(&maps.a_codes, a_codes, M, K, 128) ||
+      !encode_codes(&maps.w_codes, w_codes, N, K, block_n))
+    return SVDQ_ERR_CUDA;
+  // test hook: SVDQ_TEST_GEMM_STALL=1 makes the kernel's loader issue nothing
+  // so that its pipeline wait times out after 100 ms (status SVDQ_DEV_TIMEOUT)
+  const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
+  const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
+  cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
+                                         lora_act, L2, bias, Y, M, N, K, rank, dev_status,
+                                         test_stall, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
+svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
+                           const uint16_t* scales, const uint16_t* zeros, const uint16_t* bias,
+                           uint16_t* Y, int M, int N, int K, int group_size, int* dev_status,
+                           void* stream) {
+  (void)dev_status;  // the GEMV has no pipeline waits
+  if (M < 1 || M > 8 || N < 1 || K <= 0 || K % 128 != 0 || group_size != 64)
+    return SVDQ_ERR_SHAPE;
+  if (!X_bf16 || !qweight || !scales || !zeros || !Y) return SVDQ_ERR_NULL;
+  if (!aligned16(X_bf16) || !aligned16(qweight) || !aligned16(scales) || !aligned16(zeros) ||
+      !aligned16(Y) || (bias && !aligned16(bias)))
+    return SVDQ_ERR_ALIGN;
+  int sms = 0;
+  svdq_status st = current_device(nullptr, &sms);
+  if (st != SVDQ_OK) return st;
+  cudaError_t e = svdq::launch_awq_gemv(X_bf16, qweight, scales, zeros, bias, Y, M, N, K,
+                                        static_cast<cudaStream_t>(stream), sms);
+  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+"""Layer-level wrappers: a packed SVDQ W4A4 linear and an AWQ W4A16 linear
+holding their device buffers.  ``forward`` is the per-call path a user runs
+(two library calls for SVDQ: svdq_quantize_act then svdq_gemm_w4a4; one for
+AWQ).  Pure marshalling: buffers are torch tensors, all arithmetic is in
+libsvdq."""
+from __future__ import annotations
+
+import numpy as np
+
+from . import _lib
+
+
+class SVDQLinear:
+    """Y = svdq_gemm_w4a4(svdq_quantize_act(X)) for a weight packed once by
+    svdq_pack_weights (or given as already packed buffers)."""
+
+    def __init__(self, packed: dict, bias_bf16_bits=None, device="cuda"):
+        import torch
+
+        self.N, self.K, self.rank = packed["N"], packed["K"], packed["rank"]
+        dev = torch.device(device)
+
+        def t(a, dtype):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dtype)
+
+        self.inv_lambda = t(packed["inv_lambda"].astype(np.float32), torch.float32)
+        self.L1s = t(packed["L1s"].astype(np.uint16).view(np.int16), torch.bfloat16)
+        self.L2 = t(packed["L2"].astype(np.uint16).view(np.int16), torch.bfloat16)
+        self.w_codes = t(packed["w_codes"].astype(np.uint8), torch.uint8)
+        self.w_scales = t(packed["w_scales"].astype(np.uint8), torch.uint8)
+        self.w_tensor_scale = float(packed["w_tensor_scale"])
+        self.bias = None
+        if bias_bf16_bits is not None:
+            self.bias = t(np.asarray(bias_bf16_bits, dtype=np.uint16).view(np.int16),
+                          torch.bfloat16)
+
+    @classmethod
+    def from_float(cls, W: np.ndarray, x_absmax: np.ndarray, rank: int, bias_bf16_bits=None,
+                   device="cuda"):
+        return cls(_lib.svdq_pack_weights(W, x_absmax, rank), bias_bf16_bits, device)
+
+    def forward(self, X, out=None, act_buffers=None, dev_status=None, stream=None):
+        M = X.shape[0]
+        bufs = act_buffers or (None, None, None)
+        a_codes, a_scales, lora = _lib.svdq_quantize_act(
+            X, self.inv_lambda, self.L1s, self.rank, *bufs, dev_status=dev_status,
+            stream=stream)
+        return _lib.svdq_gemm_w4a4(a_codes, a_scales, self.w_codes, self.w_scales,
+                                   self.w_tensor_scale, lora, self.L2, self.bias, M, self.N,
+                                   self.K, self.rank, Y=out, dev_status=dev_status,
+                                   stream=stream)
+
+    __call__ = forward
+
+
+class AWQLinear:
+    """Y = awq_gemv_w4a16(X) for a weight packed by awq_pack_weights."""
+
+    def __init__(self, qweight, scales, zeros, bias_bf16_bits=None, device="cuda"):
+        import torch
+
+        dev = torch.device(device)
+        self.qweight = torch.from_numpy(np.ascontiguousarray(qweight)).to(dev)
+        self.scales = torch.from_numpy(np.ascontiguousarray(scales).view(np.int16)).to(dev)
+        self.zeros = torch.from_numpy(np.ascontiguousarray(zeros).view(np.int16)).to(dev)
+        self.bias = None
+        if bias_bf16_bits is not None:
+            self.bias = torch.from_numpy(
+                np.asarray(bias_bf16_bits, dtype=np.uint16).view(np.int16)).to(dev).view(
+                    torch.bfloat16)
+        self.N = self.qweight.shape[0]
+
+    @classmethod
+    def from_float(cls, W: np.ndarray, bias_bf16_bits=None, device="cuda"):
+        q, s, z = _lib.awq_pack_weights(W, 64)
+        return cls(q, s, z, bias_bf16_bits, device)
+
+    def forward(self, X, out=None, stream=None):
+        return _lib.awq_gemv_w4a16(X, self.qweight, self.scales, self.zeros, self.bias, 64,
+                                   Y=out, stream=stream)
+
+    __call__ = forward

@@ -1,0 +1,221 @@
+/*
+ * svdq.h -- C ABI of libsvdq: the SVDQuant W4A4 (NVFP4) linear layer of a
+ * diffusion transformer and the AWQ W4A16 modulation GEMV, for NVIDIA B300
+ * (compute capability 10.3, sm_103a).
+ *
+ * What the layer computes (source pages: news articles on "Nunchaku Lite" in
+ * Diffusers):
+ *   - dothoosh.com, "How Nunchaku Lite halves the VRAM of diffusion models",
+ *     SVDQuant paragraph: activation outliers are moved into the weights; the
+ *     hardest part of each weight matrix becomes a small 16-bit low-rank
+ *     branch; the residual is quantized to 4 bit.
+ *   - same page, fused-kernel paragraph: the low-rank down projection is fused
+ *     with the quantization kernel and the low-rank up projection with the
+ *     4-bit compute kernel.
+ *   - same page, "quantization_config" block: svdq_w4a4 precision "nvfp4",
+ *     group_size 16, rank 32; awq_w4a16 precision "int4", group_size 64;
+ *     compute_dtype "bfloat16".
+ *   - same page, kernel-family list: svdq_w4a4 for attention/MLP projections,
+ *     awq_w4a16 for the precision-sensitive, memory-bound modulation layers.
+ *   - same page, hardware list: the loader checks the device's CUDA compute
+ *     capability and raises a clear error instead of producing wrong output.
+ *
+ *   Y = Q4(X_hat) Q4(R) s_T + (X L1s) L2 + b,    X_hat = X diag(inv_lambda)
+ *
+ * Fixed rules (the pages name the formats, not the rounding):
+ *   e2m1 codes: nearest value of {0,0.5,1,1.5,2,3,4,6}, ties to the even
+ *   code, saturating at 6; the code's sign bit is the input's sign bit.
+ *   e4m3 (OCP "FN", bias 7) scales: nearest, ties to even, saturating at 448.
+ *   Activation block scale s = RNE_e4m3(amax/6) over 16 consecutive k of
+ *   x_hat = fl32(x * inv_lambda[k]); codes RNE_e2m1(x_hat / s) (exact real
+ *   quotients); a block whose s is 0 gets codes +0.  Activations carry no
+ *   tensor scale.  Weights: see svdq_pack_weights.
+ *
+ * Conventions
+ *   - Every buffer is owned by the caller.  Device calls take device
+ *     pointers (from cudaMalloc or a framework allocator) and never allocate
+ *     device memory; host calls take host pointers.
+ *   - Device calls are asynchronous and ordered on `stream` (a cudaStream_t
+ *     passed as void*; NULL is the legacy default stream).  A call that
+ *     returns an error status has launched nothing.
+ *   - bf16 / fp16 tensors are passed as uint16_t bit patterns.
+ *   - `dev_status` (nullable) is a device int the kernels write only on a
+ *     device-side condition: SVDQ_DEV_TIMEOUT if an internal pipeline wait
+ *     exceeded its bound (the kernel then abandons the tile and returns; the
+ *     output is incomplete).  Initialise it to 0; read it after the stream
+ *     synchronises.
+ *   - Device calls return SVDQ_ERR_UNSUPPORTED_ARCH unless the current device
+ *     has compute capability 10.3.
+ *   - Device pointers must be 16-byte aligned (SVDQ_ERR_ALIGN otherwise).
+ *
+ * Data layouts (device calls; the packer writes the weight side)
+ *   codes    [rows][K/2] bytes, row-major; element 2i of a row in the low
+ *            nibble of byte i, element 2i+1 in the high nibble.
+ *   scales   e4m3 bytes of a rows x C matrix (C = K/16) in 512-byte tiles:
+ *            rows form 128-row blocks rb = r/128, columns 4-column groups
+ *            cb = c/4; tile (rb, cb) starts at byte (rb*(C/4) + cb)*512 and
+ *            holds entry (r, c) at byte (r%32)*16 + ((r/32)%4)*4 + c%4.
+ *            The buffer holds ceil(rows/128) row blocks
+ *            (SVDQ_SCALE_BYTES(rows, K)); padding rows are neither written
+ *            nor used.  This is the order in which the tensor core reads
+ *            block scales, so the GEMM copies them without reshuffling.
+ *   lora     [M][rank] bf16 row-major;  L1s [K][rank] bf16;  L2 [rank][N]
+ *            bf16;  Y [M][N] bf16;  bias [N] bf16.
+ */
+#ifndef SVDQ_H_
+#define SVDQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SVDQ_OK = 0,
+  SVDQ_ERR_NULL = -1,             /* a required pointer is NULL */
+  SVDQ_ERR_SHAPE = -2,            /* a size violates the call's shape rules */
+  SVDQ_ERR_ALIGN = -3,            /* a device pointer is not 16-byte aligned */
+  SVDQ_ERR_UNSUPPORTED_ARCH = -4, /* current device is not compute capability 10.3 */
+  SVDQ_ERR_CUDA = -5,             /* a CUDA runtime/driver call failed */
+  SVDQ_ERR_RANK = -6,             /* rank not allowed for this call */
+  SVDQ_ERR_VALUE = -7,            /* a value argument is out of its domain */
+  SVDQ_ERR_NOMEM = -8             /* host scratch allocation failed (packers) */
+} svdq_status;
+
+/* values written to *dev_status by a kernel */
+#define SVDQ_DEV_OK 0
+#define SVDQ_DEV_TIMEOUT 1
+
+/* byte sizes of the packed buffers */
+#define SVDQ_CODE_BYTES(rows, K) ((size_t)(rows) * (size_t)(K) / 2)
+#define SVDQ_SCALE_BYTES(rows, K) ((((size_t)(rows) + 127) / 128) * 128 * ((size_t)(K) / 16))
+
+/* Human-readable name of a status code (static string). */
+const char* svdq_status_string(svdq_status s);
+
+/* SVDQ_OK if the current CUDA device has compute capability 10.3, else
+ * SVDQ_ERR_UNSUPPORTED_ARCH (or SVDQ_ERR_CUDA if no device can be queried).
+ * The pages' hardware list: the quantizer validates the compute capability
+ * and fails clearly rather than producing wrong output. */
+svdq_status svdq_check_device(void);
+
+/* ------------------------------------------------------------------ host */
+
+/* Calibration statistic of the smoothing step: x_absmax[j] = max_m |X[m][j]|
+ * over M rows of bf16 activations X [M][K] (host).  M may be 0 (all zeros).
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE (M < 0 or K <= 0). */
+svdq_status svdq_calib_absmax(const uint16_t* X_bf16, int64_t M, int64_t K,
+                              float* x_absmax);
+
+/* Offline packing of one nn.Linear weight W [N][K] (fp32, host, row-major)
+ * into the SVDQ W4A4 form (the SVDQuant paragraph: smoothing, 16-bit low-rank
+ * branch, 4-bit residual).  Synchronous, host only, thread-safe; allocates
+ * and frees its own host scratch.
+ *
+ *   lambda_j   = sqrt(x_absmax[j] / max_n |W[n][j]|), 1 if either is 0,
+ *                clamped to [2^-20, 2^20];  inv_lambda[j] = fl32(1/lambda_j)
+ *   W_hat^T    = diag(1/inv_lambda) W^T  (K x N, float64)
+ *   L1 L2      = rank-r truncated SVD of W_hat^T (L1 = U_r S_r, L2 = V_r^T),
+ *                by randomized subspace iteration with a Jacobi SVD of the
+ *                projected matrix (full Jacobi SVD when min(K, N) is small)
+ *   L1s        = bf16(inv_lambda[k] * L1[k][i])   -> out [K][rank]
+ *   L2         = bf16(L2)                          -> out [rank][N]
+ *   R[k][n]    = (W[n][k] - sum_{i ascending} L1s[k][i] L2[i][n]) / inv_lambda[k]
+ *                (float64, one rounding per operation, no fused multiply-add)
+ *   s_T        = smallest power of two with 6*448*s_T >= max|R| (1 if R == 0)
+ *   w_scales   = RNE_e4m3(amax16 / (6 s_T)) per 16 consecutive k of each
+ *                output channel n, in the scale tile layout (rows = N)
+ *   w_codes    = RNE_e2m1(R[k][n] / (s_b s_T)), [N][K/2] packed
+ *
+ * Sizes: N % 128 == 0, K % 128 == 0, 1 <= rank <= min(K, N).  Buffers:
+ * inv_lambda [K], L1s [K*rank], L2 [rank*N], w_codes SVDQ_CODE_BYTES(N, K),
+ * w_scales SVDQ_SCALE_BYTES(N, K), w_tensor_scale [1].
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_VALUE
+ * (non-finite W or x_absmax, or a residual beyond the float range),
+ * SVDQ_ERR_NOMEM. */
+svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absmax,
+                              int rank, float* inv_lambda, uint16_t* L1s,
+                              uint16_t* L2, uint8_t* w_codes, uint8_t* w_scales,
+                              float* w_tensor_scale);
+
+/* Offline packing of a modulation-layer weight W [N][K] (fp32, host) to AWQ
+ * W4A16 (kernel-family list: 4-bit weights, 16-bit activations; config block:
+ * int4, group_size 64).  Plain asymmetric group quantization along K, per
+ * output channel and group g of 64 consecutive k:
+ *   s = fp16((max - min) / 15), z = fp16(-min / s) clamped to +-65504,
+ *   q = clamp(RNE(w / s + z), 0, 15)  (float64 before the fp16 roundings);
+ *   a group with max == min, or whose s rounds to 0, uses s = 1, z = fp16(-min).
+ * Outputs: qweight [N][K/2] bytes (even k in the low nibble), scales and
+ * zeros [N][K/64] fp16 bit patterns.
+ * Sizes: K % 64 == 0, N >= 1, group_size == 64.
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_VALUE (non-finite W). */
+svdq_status awq_pack_weights(const float* W, int N, int K, int group_size,
+                             uint8_t* qweight, uint16_t* scales, uint16_t* zeros);
+
+/* ---------------------------------------------------------------- device */
+
+/* Activation side of the SVDQ linear, one kernel (fused-kernel paragraph:
+ * the low-rank down projection runs inside the quantization kernel).
+ * Reads X once:
+ *   lora_act[m][i] = bf16(sum_k X[m][k] L1s[k][i])   (fp32 accumulation on
+ *                    tensor cores; L1s already carries inv_lambda)
+ *   x_hat          = fl32(X[m][k] * inv_lambda[k])
+ *   a_scales       = RNE_e4m3(amax16(x_hat) / 6)   (scale tile layout, rows = M)
+ *   a_codes        = RNE_e2m1(x_hat / s)           ([M][K/2] packed)
+ * Inputs: X [M][K] bf16, inv_lambda [K] fp32, L1s [K][rank] bf16.
+ * Outputs: a_codes SVDQ_CODE_BYTES(M, K), a_scales SVDQ_SCALE_BYTES(M, K),
+ * lora_act [M][rank] bf16.
+ * Sizes: M >= 0 (M == 0 launches nothing), K % 128 == 0, rank in {16, 32, 64}.
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_ALIGN,
+ * SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA (launch failure). */
+svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
+                              const uint16_t* L1s, int M, int K, int rank,
+                              uint8_t* a_codes, uint8_t* a_scales,
+                              uint16_t* lora_act, int* dev_status, void* stream);
+
+/* The 4-bit product with the low-rank up projection and bias fused in its
+ * epilogue (fused-kernel paragraph: up projection fused with the 4-bit
+ * compute kernel):
+ *   Y = bf16( s_T * sum_k dec(a)[m][k] dec(w)[n][k]
+ *             + sum_i lora_act[m][i] L2[i][n] + bias[n] )
+ * dec(.) = e2m1 value x e4m3 block scale.  tcgen05 block-scaled NVFP4 MMA
+ * with fp32 accumulators in tensor memory; operands and scales staged by TMA.
+ * The rank-r term is accumulated on the tensor cores into the same fp32
+ * accumulator as bf16(L2[i][n] / s_T), which is exact because s_T must be a
+ * power of two (as svdq_pack_weights produces).
+ * Inputs: activation side as written by svdq_quantize_act (rows = M), weight
+ * side as written by svdq_pack_weights (rows = N), bias nullable.
+ * Output: Y [M][N] bf16.
+ * Sizes: M >= 0 (M == 0 launches nothing), N % 128 == 0, K % 128 == 0,
+ * rank in {16, 32, 64}; w_tensor_scale a finite power of two in
+ * [2^-100, 2^100] (SVDQ_ERR_VALUE otherwise).
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_VALUE,
+ * SVDQ_ERR_ALIGN, SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA. */
+svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
+                           const uint8_t* w_codes, const uint8_t* w_scales,
+                           float w_tensor_scale, const uint16_t* lora_act,
+                           const uint16_t* L2, const uint16_t* bias, uint16_t* Y,
+                           int M, int N, int K, int rank, int* dev_status,
+                           void* stream);
+
+/* AWQ W4A16 GEMV for the small-M modulation layers (kernel-family list:
+ * memory-bound adaLN modulation):
+ *   Y[m][n] = bf16( sum_k X[m][k] (q[n][k] - z[n][k/64]) s[n][k/64] + bias[n] )
+ * fp32 accumulation.  Streams the 4-bit weights once from HBM.
+ * Inputs: X [M][K] bf16; qweight [N][K/2] (even k in the low nibble);
+ * scales, zeros [N][K/64] fp16; bias [N] bf16 (nullable).  Output Y [M][N] bf16.
+ * Sizes: 1 <= M <= 8, N >= 1, K % 128 == 0, group_size == 64.
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_ALIGN,
+ * SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA. */
+svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
+                           const uint16_t* scales, const uint16_t* zeros,
+                           const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                           int group_size, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVDQ_H_ */

@@ -1,0 +1,84 @@
+"""Helpers of the GPU parity tests: moving oracle/workload arrays to the
+device in the layouts of include/svdq.h, and the output tolerance.
+
+Output tolerance (float outputs): the device rounds Y once to bf16 and
+accumulates in fp32 on tensor cores; the oracle returns Y unrounded in fp64.
+Relative Frobenius error <= 2e-3, and elementwise
+|Y_dev - Y_ref| <= 1e-2 * rms(Y_ref) + ulp_bf16(Y_ref)/2 (the half-ulp term
+covers the final bf16 rounding of large outputs)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import formats, layout
+
+REL_FRO_TOL = 2e-3
+ABS_RMS_TOL = 1e-2
+
+
+def dev_bf16(values_f32: np.ndarray) -> torch.Tensor:
+    """float32 values that are exactly bf16 -> CUDA bf16 tensor."""
+    bits = formats.bf16_bits(np.asarray(values_f32, dtype=np.float64))
+    return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_bits16(bits: np.ndarray, dtype=torch.bfloat16) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).cuda().view(
+        dtype)
+
+
+def dev_u8(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def dev_f32(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def host_bf16(t: torch.Tensor) -> np.ndarray:
+    """CUDA bf16 tensor -> float64 values."""
+    bits = t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+    return formats.bf16_from_bits(bits)
+
+
+def half_ulp_bf16(y: np.ndarray) -> np.ndarray:
+    a = np.abs(np.asarray(y, dtype=np.float64))
+    _, e = np.frexp(np.maximum(a, 2.0 ** -126))
+    return np.ldexp(1.0, e - 9)  # ulp = 2^(e-1-7); half of it
+
+
+def assert_y_close(y_dev: np.ndarray, y_ref: np.ndarray, what: str = "Y"):
+    y_dev = np.asarray(y_dev, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    assert y_dev.shape == y_ref.shape
+    assert np.all(np.isfinite(y_dev)), f"{what}: non-finite device output"
+    err = y_dev - y_ref
+    rel = np.linalg.norm(err) / max(np.linalg.norm(y_ref), 1e-300)
+    rms = np.sqrt(np.mean(y_ref ** 2)) if y_ref.size else 0.0
+    bound = ABS_RMS_TOL * rms + half_ulp_bf16(y_ref)
+    worst = np.max(np.abs(err) - bound) if err.size else -1.0
+    assert rel <= REL_FRO_TOL, f"{what}: relative Frobenius error {rel:.3e} > {REL_FRO_TOL}"
+    assert worst <= 0, (f"{what}: elementwise error exceeds 1e-2*rms + ulp/2 by {worst:.3e} "
+                        f"(max |err| {np.max(np.abs(err)):.3e}, rms {rms:.3e})")
+    return rel
+
+
+def oracle_weight_operands(packed: dict, bias_values=None) -> dict:
+    """Device buffers of the weight side from the oracle's packing."""
+    K, N = packed["K"], packed["N"]
+    out = {
+        "inv_lambda": dev_f32(packed["inv_lambda"]),
+        "L1s": dev_bits16(formats.bf16_bits(packed["L1s"]).T.copy()),     # [r][K]
+        "L2": dev_bits16(formats.bf16_bits(packed["L2"])),                 # [r][N]
+        "w_codes": dev_u8(packed["w_codes_packed"]),
+        "w_scales": dev_u8(packed["w_scales_swizzled"]),
+        "s_T": float(packed["s_T"]),
+        "bias": dev_bf16(bias_values) if bias_values is not None else None,
+        "K": K, "N": N, "rank": packed["rank"],
+    }
+    return out
+
+
+def scales_from_device(a_scales: torch.Tensor, rows: int, K: int) -> np.ndarray:
+    return layout.sf_unswizzle(a_scales.cpu().numpy(), rows, K // 16)

@@ -1,0 +1,87 @@
+"""The whole SVDQ linear on the GPU (svdq_quantize_act -> svdq_gemm_w4a4)
+against the oracle's forward on the same packed weights, for the diffusion
+transformer workloads; and the product packer's weights through the device
+path against the unquantized float64 product (quality: SVDQ beats plain
+W4A4 on outlier-heavy inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import formats, svdq
+
+import bit_w4a4_diffusion_quantize_b300 as lib
+from gpu_util import assert_y_close, dev_bf16, host_bf16, oracle_weight_operands
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_forward(X, w, rank):
+    M, K = X.shape
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, lora = lib.svdq_quantize_act(dev_bf16(X), w["inv_lambda"], w["L1s"], rank,
+                                                dev_status=status)
+    Y = lib.svdq_gemm_w4a4(codes, scales, w["w_codes"], w["w_scales"], w["s_T"], lora, w["L2"],
+                           w["bias"], M, w["N"], K, rank, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return Y, codes, scales, lora
+
+
+def _oracle_case(case, X=None, W=None, b=None):
+    if X is None:
+        X = workloads.make_activations(case)
+    if W is None:
+        W, b = workloads.make_weights(case)
+    packed = svdq.pack_weights(W, svdq.calib_absmax(X), case.rank)
+    return X, W, b, packed, svdq.linear_forward(X, packed, b)
+
+
+@pytest.mark.parametrize("name", ["tiny", "attn_out", "qkv"])
+def test_linear_parity(name):
+    case = workloads.CASES[name]
+    X, W, b, packed, out = _oracle_case(case)
+    Y, codes, _, _ = _device_forward(X, oracle_weight_operands(packed, b), case.rank)
+    assert np.array_equal(codes.cpu().numpy(), out["a_codes_packed"])
+    assert_y_close(host_bf16(Y), out["Y"], name)
+
+
+def test_linear_ragged():
+    case = workloads.custom_case(333, 640, 384, 32, seed=21)
+    X, W, b, packed, out = _oracle_case(case)
+    Y, _, _, _ = _device_forward(X, oracle_weight_operands(packed, b), 32)
+    assert_y_close(host_bf16(Y), out["Y"])
+
+
+def test_mlp_pair_fc1_gelu_fc2():
+    """fc1 (4096 x 3072 -> 12288), GELU (tanh) on fc1's oracle output rounded
+    to bf16, fc2 (12288 -> 3072); fc2's own smoothing comes from its input."""
+    c1 = workloads.CASES["fc1"]
+    X1, W1, b1, p1, o1 = _oracle_case(c1)
+    Y1, _, _, _ = _device_forward(X1, oracle_weight_operands(p1, b1), c1.rank)
+    assert_y_close(host_bf16(Y1), o1["Y"], "fc1")
+    X2 = svdq.gelu_tanh_bf16(formats.round_to_bf16(o1["Y"])).astype(np.float32)
+    c2 = workloads.CASES["fc2"]
+    W2, b2 = workloads.make_fc2_weights(c2)
+    _, _, _, p2, o2 = _oracle_case(c2, X2, W2, b2)
+    Y2, _, _, _ = _device_forward(X2, oracle_weight_operands(p2, b2), c2.rank)
+    assert_y_close(host_bf16(Y2), o2["Y"], "fc2")
+
+
+def test_product_packer_quality_through_device():
+    """Weights packed by svdq_pack_weights, run through the device path: the
+    error against float64 X W^T + b is below plain W4A4's (oracle) and within
+    10% of the oracle's own SVDQ error."""
+    case = workloads.custom_case(1024, 1024, 1024, 32, seed=31, outlier_scale=50.0)
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    exact = X.astype(np.float64) @ W.T.astype(np.float64) + b
+    layer = lib.SVDQLinear.from_float(W, lib.svdq_calib_absmax(workloads.bf16_bits_of(X)), 32,
+                                      workloads.bf16_bits_of(b))
+    y = host_bf16(layer(dev_bf16(X)))
+    nrm = np.linalg.norm(exact)
+    e_dev = np.linalg.norm(y - exact) / nrm
+    e_naive = np.linalg.norm(svdq.naive_w4a4(X, W, b) - exact) / nrm
+    e_oracle = np.linalg.norm(_oracle_case(case, X, W, b)[4]["Y"] - exact) / nrm
+    assert e_dev < 0.5 * e_naive, (e_dev, e_naive)
+    assert e_dev < 1.1 * e_oracle + 2e-3, (e_dev, e_oracle)

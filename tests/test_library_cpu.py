@@ -1,0 +1,205 @@
+"""libsvdq on the CPU: the library loads and exports every symbol the C
+headers declare; host-detectable argument errors of the device calls; the
+host packers against the oracle (bit-exact where the result is unique,
+validity where it is not: the SVD factors are unique only up to rotation and
+rounding, so the packed codes are checked to be exactly the quantization of
+the residual of the packer's own factors)."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import awq, formats, layout, svdq
+
+import bit_w4a4_diffusion_quantize_b300 as lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HAS_GPU = torch.cuda.is_available()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "awq_gemv_w4a16",
+            "awq_pack_weights", "svdq_calib_absmax", "svdq_check_device",
+            "svdq_status_string"} <= names
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings():
+    for st in range(-8, 1):
+        s = lib.raw_lib().svdq_status_string(st).decode()
+        assert s.startswith(lib.status_name(st))
+
+
+def test_check_device_status_is_defined():
+    st = lib.check_device()
+    if HAS_GPU:
+        assert st in (0, -4)
+    else:
+        assert st == -5  # no device to query
+
+
+# ------------------------------------------------------------- argument errors
+P = ctypes.c_void_p
+ALIGNED = P(0x10000)      # never dereferenced: every case below fails validation
+MISALIGNED = P(0x10008)
+
+
+def _qa(X=ALIGNED, inv=ALIGNED, l1=ALIGNED, M=64, K=256, r=32, codes=ALIGNED, sc=ALIGNED,
+        lora=ALIGNED):
+    return lib.raw_lib().svdq_quantize_act(X, inv, l1, M, K, r, codes, sc, lora, None, None)
+
+
+def _gemm(M=64, N=256, K=256, r=32, sT=2.0 ** -10, Y=ALIGNED, a=ALIGNED, bias=None):
+    return lib.raw_lib().svdq_gemm_w4a4(a, ALIGNED, ALIGNED, ALIGNED, ctypes.c_float(sT),
+                                        ALIGNED, ALIGNED, bias, Y, M, N, K, r, None, None)
+
+
+def _awq(M=1, N=64, K=256, g=64, X=ALIGNED):
+    return lib.raw_lib().awq_gemv_w4a16(X, ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, M, N, K, g,
+                                        None, None)
+
+
+def test_quantize_act_argument_errors():
+    assert _qa(K=200) == -2 and _qa(K=0) == -2 and _qa(M=-1) == -2
+    assert _qa(r=8) == -6 and _qa(r=48) == -6
+    assert _qa(X=P(0)) == -1 and _qa(lora=P(0)) == -1
+    assert _qa(X=MISALIGNED) == -3 and _qa(sc=MISALIGNED) == -3
+    assert _qa(M=0, X=P(0)) == 0  # empty input: nothing to do
+
+
+def test_gemm_argument_errors():
+    assert _gemm(N=200) == -2 and _gemm(K=200) == -2 and _gemm(M=-3) == -2
+    assert _gemm(r=24) == -6
+    assert _gemm(sT=3.0) == -7 and _gemm(sT=float("inf")) == -7 and _gemm(sT=0.0) == -7
+    assert _gemm(sT=2.0 ** -101) == -7 and _gemm(sT=2.0 ** 101) == -7
+    assert _gemm(Y=P(0)) == -1
+    assert _gemm(a=MISALIGNED) == -3 and _gemm(bias=MISALIGNED) == -3
+    assert _gemm(M=0, Y=P(0)) == 0
+
+
+def test_awq_argument_errors():
+    assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(K=192) == -2 and _awq(g=128) == -2
+    assert _awq(N=0) == -2
+    assert _awq(X=P(0)) == -1 and _awq(X=MISALIGNED) == -3
+
+
+@pytest.mark.skipif(HAS_GPU, reason="valid arguments would launch on a real device")
+def test_device_calls_without_device_report_cuda_error():
+    assert _qa() == -5 and _gemm() == -5 and _awq() == -5
+
+
+# ------------------------------------------------------------- host packers
+def test_calib_absmax_matches_oracle():
+    case = workloads.CASES["tiny"]
+    X = workloads.make_activations(case)
+    got = lib.svdq_calib_absmax(workloads.bf16_bits_of(X))
+    assert np.array_equal(got, svdq.calib_absmax(X))
+    assert np.array_equal(lib.svdq_calib_absmax(np.zeros((0, 128), np.uint16)), np.zeros(128))
+
+
+def _packer_case(case):
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    xm = svdq.calib_absmax(X)
+    return X, W, xm, lib.svdq_pack_weights(W, xm, case.rank)
+
+
+@pytest.mark.parametrize("case", [
+    workloads.CASES["tiny"],                                 # direct Jacobi SVD path
+    workloads.custom_case(256, 512, 384, 32, seed=3),        # randomized subspace path
+    workloads.custom_case(64, 384, 640, 16, seed=4),         # N > K
+], ids=lambda c: f"{c.name}-{c.N}x{c.K}-r{c.rank}")
+def test_packer_matches_oracle(case):
+    X, W, xm, p = _packer_case(case)
+    # unique parts: smoothing factors
+    assert np.array_equal(p["inv_lambda"], svdq.smoothing_inv_lambda(xm, W))
+    # factors are bf16; the residual of the packer's own factors, quantized by
+    # the oracle, must equal the packer's codes, scales and tensor scale
+    L1s = formats.bf16_from_bits(p["L1s"]).T
+    L2 = formats.bf16_from_bits(p["L2"])
+    R = svdq.residual(W, p["inv_lambda"], L1s, L2)
+    sT = svdq.tensor_scale(R)
+    codes, sc = svdq.quantize_weight_residual(R, sT)
+    assert p["w_tensor_scale"] == sT
+    assert np.array_equal(p["w_codes"], layout.pack_nibbles(codes))
+    assert np.array_equal(p["w_scales"], layout.sf_swizzle(sc))
+    # the low-rank branch is near-optimal: residual within 1% of the residual
+    # left by LAPACK's exact top-r factors (both with bf16 factors)
+    ref = svdq.pack_weights(W, xm, case.rank)
+    assert np.linalg.norm(R) <= 1.01 * np.linalg.norm(ref["R"])
+
+
+def test_packer_full_rank_leaves_rounding_residual():
+    case = workloads.custom_case(32, 128, 128, 128, seed=6, outlier_channels=2,
+                                 planted_rank=8)
+    X, W, xm, p = _packer_case(case)
+    L1s = formats.bf16_from_bits(p["L1s"]).T
+    L2 = formats.bf16_from_bits(p["L2"])
+    W_hat = W.T.astype(np.float64) / p["inv_lambda"].astype(np.float64)[:, None]
+    R = svdq.residual(W, p["inv_lambda"], L1s, L2)
+    # only the bf16 rounding of the factors is left
+    assert np.linalg.norm(R) <= 2.0 ** -7 * np.linalg.norm(W_hat)
+
+
+def test_packer_argument_errors():
+    W = np.zeros((128, 128), np.float32)
+    xm = np.ones(128, np.float32)
+    with pytest.raises(lib.SvdqError) as e:
+        lib.svdq_pack_weights(np.zeros((100, 128), np.float32), xm, 16)
+    assert e.value.status == -2
+    with pytest.raises(lib.SvdqError) as e:
+        lib.svdq_pack_weights(W, xm, 0)
+    assert e.value.status == -6
+    with pytest.raises(lib.SvdqError) as e:
+        lib.svdq_pack_weights(W, xm, 129)
+    assert e.value.status == -6
+    Wn = W.copy()
+    Wn[3, 5] = np.nan
+    with pytest.raises(lib.SvdqError) as e:
+        lib.svdq_pack_weights(Wn, xm, 16)
+    assert e.value.status == -7
+
+
+def test_packer_zero_weight():
+    p = lib.svdq_pack_weights(np.zeros((128, 128), np.float32), np.ones(128, np.float32), 16)
+    assert p["w_tensor_scale"] == 1.0
+    assert not p["w_codes"].any() and not p["w_scales"].any()
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (37, 192), (1, 64)])
+def test_awq_packer_matches_oracle(N, K):
+    rng = np.random.default_rng(N + K)
+    W = rng.standard_normal((N, K)).astype(np.float32) * 0.02
+    W[0, :64] = 0.5           # a constant group
+    if N > 1:
+        W[1, 64:128 if K >= 128 else 64] = 0.0
+    q, s, z = lib.awq_pack_weights(W)
+    o = awq.awq_pack(W)
+    assert np.array_equal(q, o["qweight"])
+    assert np.array_equal(s, o["scales_bits"])
+    assert np.array_equal(z, o["zeros_bits"])
+
+
+def test_awq_packer_errors():
+    with pytest.raises(lib.SvdqError):
+        lib.awq_pack_weights(np.zeros((4, 100), np.float32))
+    with pytest.raises(lib.SvdqError):
+        lib.awq_pack_weights(np.full((4, 64), np.inf, np.float32))
