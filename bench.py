@@ -78,28 +78,33 @@ def barrier(world: int):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons with
+    nvidia-smi every 50 ms while the timed loop and its repeats run
+    (read-only queries: no setting of the GPU is changed)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
             self.proc = None
+        self.t0 = time.perf_counter()
         return self
 
     def _read(self):
@@ -107,6 +112,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self.t1 = time.perf_counter()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -117,24 +123,25 @@ class ClockSampler:
                 self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, power, mx, reasons = [], [], None, set()
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 7:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                power.append(float(parts[2]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(self.REASONS, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None,
+                "window_s": round(self.t1 - self.t0, 3), "source": "nvidia-smi, 50 ms period"}
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
@@ -190,7 +197,7 @@ def run_gpu(args, world, rank, local):
             "X": dbits(Xbits).view(torch.bfloat16).view(M, K),
             "inv": torch.from_numpy(packed["inv_lambda"]).to(dev),
             "L1s": dbits(packed["L1s"]).view(torch.bfloat16),
-            "L2": dbits(packed["L2"]).view(torch.bfloat16),
+            "L2s": dbits(packed["L2s"]).view(torch.bfloat16),
             "wc": torch.from_numpy(packed["w_codes"]).to(dev),
             "ws": torch.from_numpy(packed["w_scales"]).to(dev),
             "bias": dbits(workloads.bf16_bits_of(b)).view(torch.bfloat16),
@@ -212,17 +219,16 @@ def run_gpu(args, world, rank, local):
                               dev_status=status, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        lib.svdq_gemm_w4a4(s["ac"], s["as"], s["wc"], s["ws"], sT, s["lora"], s["L2"],
+        lib.svdq_gemm_w4a4(s["ac"], s["as"], s["wc"], s["ws"], sT, s["lora"], s["L2s"],
                            s["bias"], M, N, K, r, Y=s["Y"], dev_status=status, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
         barrier(world)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
@@ -231,6 +237,16 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         barrier(world)
+        # the timed loop above lasts milliseconds; keep the same loads running
+        # (untimed repeats of the identical step) so the clock record spans
+        # at least one second of this work
+        t_end = time.perf_counter() + max(0.0, 1.0 - wall)
+        i = 0
+        while time.perf_counter() < t_end:
+            for _ in range(64):
+                step(i)
+                i += 1
+            torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError("device status set during the timed region")
     t_q = [evs[i][0].elapsed_time(evs[i][1]) * 1e-3 for i in range(args.steps)]

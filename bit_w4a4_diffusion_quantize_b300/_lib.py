@@ -48,6 +48,7 @@ _SIGS = {
                               _i32, _i32, _i32, _c_p, _c_p]),
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
+    "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -105,22 +106,24 @@ def svdq_calib_absmax(X_bf16_bits: np.ndarray) -> np.ndarray:
 
 def svdq_pack_weights(W: np.ndarray, x_absmax: np.ndarray, rank: int) -> dict:
     """Offline packing of an nn.Linear weight W [N, K] (float32).  Returns the
-    device-side buffers as NumPy arrays."""
+    device-side buffers as NumPy arrays: inv_lambda [K] fp32, L1s [rank, K]
+    and L2s [N, rank] bf16 bits (L2s = L2^T / s_T), w_codes [N, K/2],
+    w_scales (tile layout), w_tensor_scale."""
     W = np.ascontiguousarray(W, dtype=np.float32)
     xm = np.ascontiguousarray(x_absmax, dtype=np.float32)
     N, K = W.shape
     r = max(int(rank), 0)
     inv = np.zeros(K, dtype=np.float32)
     L1s = np.zeros((r, K), dtype=np.uint16)
-    L2 = np.zeros((r, N), dtype=np.uint16)
+    L2s = np.zeros((N, r), dtype=np.uint16)
     codes = np.zeros((N, K // 2), dtype=np.uint8)
     scales = np.zeros(scale_bytes(N, K), dtype=np.uint8)
     sT = np.zeros(1, dtype=np.float32)
     st = _lib.svdq_pack_weights(_np_ptr(W), N, K, _np_ptr(xm), int(rank), _np_ptr(inv),
-                                _np_ptr(L1s), _np_ptr(L2), _np_ptr(codes), _np_ptr(scales),
+                                _np_ptr(L1s), _np_ptr(L2s), _np_ptr(codes), _np_ptr(scales),
                                 _np_ptr(sT))
     _check(st, "svdq_pack_weights")
-    return {"N": N, "K": K, "rank": int(rank), "inv_lambda": inv, "L1s": L1s, "L2": L2,
+    return {"N": N, "K": K, "rank": int(rank), "inv_lambda": inv, "L1s": L1s, "L2s": L2s,
             "w_codes": codes, "w_scales": scales, "w_tensor_scale": float(sT[0])}
 
 
@@ -153,8 +156,11 @@ def _stream_ptr(stream):
 
 
 def _check_cuda(t, name):
-    if t is not None and not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if t is not None:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (the library reads raw row-major memory)")
 
 
 def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None,
@@ -179,18 +185,18 @@ def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None
     return a_codes, a_scales, lora_act
 
 
-def svdq_gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act, L2,
+def svdq_gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act, L2s,
                    bias, M: int, N: int, K: int, rank: int, Y=None, dev_status=None,
                    stream=None):
-    """Returns Y [M, N] bf16 (CUDA)."""
+    """L2s: [N, rank] bf16 = L2^T / s_T.  Returns Y [M, N] bf16 (CUDA)."""
     torch = _torch()
     for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
-                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2, "L2"), (bias, "bias")):
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias")):
         _check_cuda(t, n)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
     st = _lib.svdq_gemm_w4a4(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales),
-                             float(w_tensor_scale), _dptr(lora_act), _dptr(L2), _dptr(bias),
+                             float(w_tensor_scale), _dptr(lora_act), _dptr(L2s), _dptr(bias),
                              _dptr(Y), int(M), int(N), int(K), int(rank), _dptr(dev_status),
                              _stream_ptr(stream))
     _check(st, "svdq_gemm_w4a4")
@@ -213,3 +219,10 @@ def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None
                              _dptr(dev_status), _stream_ptr(stream))
     _check(st, "awq_gemv_w4a16")
     return Y
+
+
+def bench_mma_rate(mode: int, n: int, iters: int, ctas: int, dev_status=None, stream=None):
+    """Launch the tensor-core rate kernel (include/svdq_bench.h); time it with
+    CUDA events on `stream`."""
+    _check(_lib.svdq_bench_mma_rate(int(mode), int(n), int(iters), int(ctas), _dptr(dev_status),
+                                    _stream_ptr(stream)), "svdq_bench_mma_rate")

@@ -17,7 +17,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsvdq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu"]
+CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu", "microbench.cu"]
 HOST_SOURCES = ["pack.cpp"]
 HEADERS = ["device_common.cuh", "launch.h"]
 
@@ -53,7 +53,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     """Compile every source that changed and link libsvdq.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "svdq.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "svdq.h"),
+                                                       os.path.join(INCLUDE, "svdq_bench.h")]
     objs = []
     for src in CUDA_SOURCES:
         s = os.path.join(CSRC, src)

@@ -90,17 +90,35 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows][K/2] bytes of 4-bit codes; box = 128 bytes x box_rows, 128B swizzle
-bool encode_codes(CUtensorMap* map, const uint8_t* ptr, int rows, int K, int box_rows) {
+// 2-D row-major tensor of `rows` rows x `inner` elements (row pitch
+// `pitch_bytes`), box `box_inner` x `box_rows`, with the given swizzle
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner,
+               uint64_t rows, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows][K/2] bytes of 4-bit codes: box 128 bytes x box_rows, 128B swizzle
+bool encode_codes(CUtensorMap* map, const uint8_t* ptr, int rows, int K, int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, (uint64_t)K / 2, (uint64_t)rows,
+                   (uint64_t)K / 2, 128u, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// [rows][rank] bf16 rank-r operand: one row per box line, swizzle span = row bytes
+bool encode_rank_rows(CUtensorMap* map, const uint16_t* ptr, int rows, int rank, int box_rows) {
+  const CUtensorMapSwizzle sw = rank == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rank == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, ptr, (uint64_t)rank, (uint64_t)rows,
+                   (uint64_t)rank * 2, (uint32_t)rank, (uint32_t)box_rows, sw);
 }
 
 }  // namespace
@@ -137,18 +155,21 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
   if (!aligned16(X_bf16) || !aligned16(inv_lambda) || !aligned16(L1s) || !aligned16(a_codes) ||
       !aligned16(a_scales) || !aligned16(lora_act))
     return SVDQ_ERR_ALIGN;
-  int sms = 0;
-  svdq_status st = current_device(nullptr, &sms);
+  svdq_status st = current_device(nullptr, nullptr);
   if (st != SVDQ_OK) return st;
-  cudaError_t e = svdq::launch_quantize_act(X_bf16, inv_lambda, L1s, M, K, rank, a_codes,
+  CUtensorMap tm_x;
+  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, X_bf16, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)K * 2, 64u, 16u, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SVDQ_ERR_CUDA;
+  cudaError_t e = svdq::launch_quantize_act(tm_x, L1s, inv_lambda, M, K, rank, a_codes,
                                             a_scales, lora_act, dev_status,
-                                            static_cast<cudaStream_t>(stream), sms);
+                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 
 svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
                            const uint8_t* w_codes, const uint8_t* w_scales,
-                           float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2,
+                           float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2s,
                            const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
                            int* dev_status, void* stream) {
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
@@ -161,26 +182,29 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
       return SVDQ_ERR_VALUE;
   }
   if (M == 0) return SVDQ_OK;
-  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2 || !Y)
+  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2s || !Y)
     return SVDQ_ERR_NULL;
   if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
-      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2) || !aligned16(Y) ||
+      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2s) || !aligned16(Y) ||
       (bias && !aligned16(bias)))
     return SVDQ_ERR_ALIGN;
-  svdq_status st = current_device(nullptr, nullptr);
+  int sms = 0;
+  svdq_status st = current_device(nullptr, &sms);
   if (st != SVDQ_OK) return st;
   const int block_n = (N % 256 == 0) ? 256 : 128;
   svdq::GemmMaps maps;
   if (!encode_codes(&maps.a_codes, a_codes, M, K, 128) ||
-      !encode_codes(&maps.w_codes, w_codes, N, K, block_n))
+      !encode_codes(&maps.w_codes, w_codes, N, K, block_n) ||
+      !encode_rank_rows(&maps.lora, lora_act, M, rank, 128) ||
+      !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n))
     return SVDQ_ERR_CUDA;
   // test hook: SVDQ_TEST_GEMM_STALL=1 makes the kernel's loader issue nothing
   // so that its pipeline wait times out after 100 ms (status SVDQ_DEV_TIMEOUT)
   const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
   const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
-                                         lora_act, L2, bias, Y, M, N, K, rank, dev_status,
-                                         test_stall, static_cast<cudaStream_t>(stream));
+                                         bias, Y, M, N, K, rank, dev_status, test_stall, sms,
+                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 
@@ -188,8 +212,8 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
                            const uint16_t* scales, const uint16_t* zeros, const uint16_t* bias,
                            uint16_t* Y, int M, int N, int K, int group_size, int* dev_status,
                            void* stream) {
-  (void)dev_status;  // the GEMV has no pipeline waits
-  if (M < 1 || M > 8 || N < 1 || K <= 0 || K % 128 != 0 || group_size != 64)
+  if (M < 1 || M > 8 || N < 8 || N % 8 != 0 || K <= 0 || K % 128 != 0 ||
+      K > svdq::awq_max_k() || group_size != 64)
     return SVDQ_ERR_SHAPE;
   if (!X_bf16 || !qweight || !scales || !zeros || !Y) return SVDQ_ERR_NULL;
   if (!aligned16(X_bf16) || !aligned16(qweight) || !aligned16(scales) || !aligned16(zeros) ||
@@ -198,8 +222,12 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
   int sms = 0;
   svdq_status st = current_device(nullptr, &sms);
   if (st != SVDQ_OK) return st;
-  cudaError_t e = svdq::launch_awq_gemv(X_bf16, qweight, scales, zeros, bias, Y, M, N, K,
-                                        static_cast<cudaStream_t>(stream), sms);
+  CUtensorMap tm_q;
+  if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
+                 (uint64_t)K / 2, 128u, 16u, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SVDQ_ERR_CUDA;
+  cudaError_t e = svdq::launch_awq_gemv(tm_q, X_bf16, scales, zeros, bias, Y, M, N, K,
+                                        dev_status, static_cast<cudaStream_t>(stream), sms);
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 

@@ -131,15 +131,29 @@ SVDQ_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
       "r"(bytes)
       : "memory");
 }
+// Suspend-time hint of mbarrier.try_wait in ns (0: the instruction's default).
+#ifndef SVDQ_TRY_WAIT_HINT_NS
+#define SVDQ_TRY_WAIT_HINT_NS 0
+#endif
 SVDQ_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#if SVDQ_TRY_WAIT_HINT_NS > 0
   asm volatile(
       "{\n.reg .pred p;\n"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)SVDQ_TRY_WAIT_HINT_NS)
       : "memory");
+#else
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 // Bounded wait on an mbarrier phase.  Returns false (and reports) on timeout.
@@ -249,6 +263,20 @@ SVDQ_DEVINL void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 SVDQ_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// each thread of the warp stores 4 consecutive 32-bit columns of its lane
+SVDQ_DEVINL void tmem_st_32x32b_x4(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+SVDQ_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+SVDQ_DEVINL uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), fixed version field 1 at bit 46, layout

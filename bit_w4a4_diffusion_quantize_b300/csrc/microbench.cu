@@ -1,0 +1,101 @@
+// Tensor-core rate measurement for the roofline of svdq_gemm_w4a4: every CTA
+// (one per SM) issues `iters` tcgen05 MMAs back to back on operands resident
+// in shared memory (zeros), accumulating into one TMEM accumulator, and waits
+// for completion.  No global memory traffic; the host times the launch.
+//
+// mode 0: kind::mxf4nvf4 block-scaled NVFP4 (M=128, N=n, K=64, ue4m3 scales)
+// mode 1: kind::f16 bf16 (M=128, N=n, K=16)
+// mode 2: mode 0 plus the tcgen05.cp of the scale chunks before every MMA
+//         (as the GEMM issues them)
+#include <cstdint>
+
+#include "../../include/svdq_bench.h"
+#include "device_common.cuh"
+
+namespace svdq {
+namespace {
+
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_mma_rate(int mode, int n, int iters, int* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // A 128 x 128 B, B n x 128 B (128B swizzle), scales 4 KB, barrier, tmem slot
+  uint8_t* A = smem;
+  uint8_t* B = smem + 16384;
+  uint8_t* SF = B + 32768;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(SF + 4096);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(SF + 4096 + 8);
+  for (int i = threadIdx.x; i < (16384 + 32768 + 4096) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (threadIdx.x == 0) {
+    const uint32_t a = smem_u32(A), b = smem_u32(B), sf = smem_u32(SF);
+    const uint32_t idesc_nvf4 =
+        (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    const uint32_t idesc_bf16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    const uint32_t sfa = tmem + 256, sfb = tmem + 256 + 4;
+    for (int i = 0; i < iters; ++i) {
+      const uint32_t koff = (uint32_t)(i & 3) * 32;
+      if (mode == 1) {
+        tc_mma_bf16(tmem, smem_desc(a + koff, 16, 1024, kSwizzle128B),
+                    smem_desc(b + koff, 16, 1024, kSwizzle128B), idesc_bf16, i > 0 ? 1u : 0u);
+      } else {
+        if (mode == 2) {
+          tc_cp_32x128b_warpx4(sfa, smem_desc(sf, 128, 128, kSwizzleNone));
+          for (int h = 0; h < n / 128; ++h)
+            tc_cp_32x128b_warpx4(sfb + 4 * h, smem_desc(sf + 512 * (h + 1), 128, 128,
+                                                        kSwizzleNone));
+        }
+        tc_mma_nvf4(tmem, smem_desc(a + koff, 16, 1024, kSwizzle128B),
+                    smem_desc(b + koff, 16, 1024, kSwizzle128B), idesc_nvf4, sfa, sfb,
+                    i > 0 ? 1u : 0u);
+      }
+    }
+    tc_commit(bar);
+    mbar_wait(bar, 0, dev_status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+}  // namespace svdq
+
+extern "C" svdq_status svdq_bench_mma_rate(int mode, int n, int iters, int ctas,
+                                           int* dev_status, void* stream) {
+  if (mode < 0 || mode > 2 || (n != 128 && n != 256) || iters < 1 || ctas < 1)
+    return SVDQ_ERR_SHAPE;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SVDQ_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return SVDQ_ERR_UNSUPPORTED_ARCH;
+  const int smem = 16384 + 32768 + 4096 + 64 + 1024;
+  if (cudaFuncSetAttribute(svdq::k_mma_rate, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return SVDQ_ERR_CUDA;
+  svdq::k_mma_rate<<<ctas, svdq::kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      mode, n, iters, dev_status);
+  return cudaGetLastError() == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}

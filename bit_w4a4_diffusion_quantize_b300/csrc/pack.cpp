@@ -412,11 +412,11 @@ svdq_status svdq_calib_absmax(const uint16_t* X_bf16, int64_t M, int64_t K, floa
 }
 
 svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absmax, int rank,
-                              float* inv_lambda, uint16_t* L1s, uint16_t* L2,
+                              float* inv_lambda, uint16_t* L1s, uint16_t* L2s,
                               uint8_t* w_codes, uint8_t* w_scales, float* w_tensor_scale) {
   if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
   if (rank < 1 || rank > std::min(N, K)) return SVDQ_ERR_RANK;
-  if (!W || !x_absmax || !inv_lambda || !L1s || !L2 || !w_codes || !w_scales || !w_tensor_scale)
+  if (!W || !x_absmax || !inv_lambda || !L1s || !L2s || !w_codes || !w_scales || !w_tensor_scale)
     return SVDQ_ERR_NULL;
   if (!all_finite(W, (size_t)N * K) || !all_finite(x_absmax, (size_t)K)) return SVDQ_ERR_VALUE;
   for (int k = 0; k < K; ++k)
@@ -456,7 +456,6 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
       for (int n = 0; n < N; ++n) l2[(size_t)i * N + n] = bf16_from_double(U.col(i)[n]);
     }
     std::memcpy(L1s, l1s.data(), l1s.size() * sizeof(uint16_t));
-    std::memcpy(L2, l2.data(), l2.size() * sizeof(uint16_t));
     std::vector<double> l1d((size_t)rank * K), l2d((size_t)rank * N);
     for (size_t i = 0; i < l1d.size(); ++i) l1d[i] = bf16_to_double(l1s[i]);
     for (size_t i = 0; i < l2d.size(); ++i) l2d[i] = bf16_to_double(l2[i]);
@@ -496,6 +495,10 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
       return SVDQ_ERR_VALUE;
     }
     *w_tensor_scale = (float)sT;
+    // L2s[n][i] = bf16(L2)[i][n] / s_T: exact, s_T is a power of two
+    for (int n = 0; n < N; ++n)
+      for (int i = 0; i < rank; ++i)
+        L2s[(size_t)n * rank + i] = bf16_from_double(l2d[(size_t)i * N + n] / sT);
     // (5) block scales and codes, 16 consecutive k of one output channel
     const size_t C = (size_t)K / 16;
     parallel_for(NN, [&](int64_t b, int64_t e) {

@@ -5,27 +5,35 @@
 //
 //   lora_act[m][i] = bf16( sum_k X[m][k] L1s[i][k] )      tensor cores, fp32 acc
 //   x_hat          = fl32( X[m][k] * inv_lambda[k] )
-//   scale byte     = RNE_e4m3( amax16(x_hat) / 6 )        IEEE fp32 division
+//   scale byte     = RNE_e4m3( amax16(x_hat) / 6 )        exact quotient rounding
 //   code nibble    = RNE_e2m1( x_hat / s )                exact quotient rounding
 //
-// Work split.  A CTA owns 16*MT consecutive rows (MT m16 tiles) and all of K;
-// its 8 warps split K into contiguous ranges of 64-wide steps.  In one step a
-// thread (quad lane t, group g) holds 16 consecutive k of rows g, g+8 (+16,
-// +24): exactly one 16-element quantization block per row, read with 128-bit
-// loads.  The same registers are the A fragments of the m16n8k16 MMAs of the
+// Work split.  A CTA owns 16 consecutive rows (one m16 tile) and all of K; its
+// 8 warps split K into contiguous ranges of 64-wide steps.  Each warp streams
+// its X range through a private TMA ring in shared memory: per step one
+// 16 x 64 bf16 tile of X (128-byte swizzle, so the fragment reads below are
+// free of bank conflicts) and the 64 matching floats of inv_lambda, landing on
+// one mbarrier.  In one step a thread (quad lane t, group g) holds 16
+// consecutive k of rows g and g+8: exactly one 16-element quantization block
+// per row.  The same registers are the A fragments of the m16n8k16 MMAs of the
 // down projection; the k order inside an MMA is permuted, and the B fragments
-// (L1s rows, k contiguous) are read with the same permutation, so no data is
-// moved between lanes.  Partial lora sums of the 8 warps are added in a fixed
-// order through shared memory, then rounded once to bf16.
+// (L1s rows, k contiguous, read from L2 one step ahead) use the same
+// permutation.  Partial lora sums of the 8 warps are added in a fixed order
+// through shared memory, then rounded once.
 //
-// Quotient x_hat / s.  s is an e4m3 value (4 significant bits).  With
-// r_hi = RD(1/s) and r_lo = RN((1 - r_hi s) / s) (the residual 1 - r_hi s is
-// exact through one fma), y = RN(x r_hi + RN(x r_lo)) differs from the exact
-// quotient by less than 2^-46 of it.  The exact quotient is either an e2m1
-// midpoint m itself or more than 0.53 ulp(m) away from it (x_hat has 24
-// significant bits, m*s at most 7), so y rounds to the same e2m1 code as the
-// exact quotient.  r_hi rounds down so that r_lo >= 0 and y keeps the sign of
-// x_hat even for -0.  Blocks whose amax is infinite take IEEE division.
+// Exact quotients without division.  For a divisor d with few significant
+// bits (6 for the scale, an e4m3 value s for the codes), take r_hi = RD(1/d)
+// and r_lo = RN((1 - r_hi d) / d) (the residual 1 - r_hi d is exact through
+// one fma).  Then y = RN(x r_hi + RN(x r_lo)) differs from x/d by less than
+// 2^-46 of it.  An exact quotient of a 24-bit x is either a grid midpoint m
+// itself or more than half an ulp of m away from it (for d = s, x_hat/s vs the
+// e2m1 midpoints: at least 0.53 ulp(m); for d = 6, amax/6 vs the e4m3
+// midpoints: at least 0.66 ulp(m)), so y rounds (RNE, satfinite) to the same
+// grid point as the exact quotient.  r_hi rounds down so that r_lo >= 0 and y
+// keeps the sign of x_hat even for -0.  The reciprocal pairs of the 127
+// positive e4m3 values are tabulated per CTA.  A block holding +-inf gets
+// s = 448 (saturated), r_lo > 0, so inf stays inf and saturates to +-6, which
+// is the exact rounding too.  A block whose s is 0 is masked to codes +0.
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -37,10 +45,33 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;
 
-// quantize one 16-element block held by one thread (8 bf16x2 words)
-SVDQ_DEVINL void quant_block16(const uint32_t (&w)[8], const float (&inv)[16], uint2& codes,
-                               uint32_t& sbyte) {
+template <int RANK>
+struct QCfg {
+  static constexpr int NT = RANK / 8;         // n8 tiles of the down projection
+  static constexpr int X_BYTES = 16 * 128;    // 16 rows x 64 bf16
+  static constexpr int INV_BYTES = 64 * 4;
+  static constexpr int TX_BYTES = X_BYTES + INV_BYTES;
+  static constexpr int OFF_X = 0;                                   // [warps][stages] tiles
+  static constexpr int OFF_INV = kWarps * kStages * X_BYTES;        // [warps][stages] slices
+  static constexpr int OFF_TAB = OFF_INV + kWarps * kStages * INV_BYTES;  // [128] float2
+  static constexpr int OFF_BAR = OFF_TAB + 128 * 8;
+  static constexpr int OFF_RED = OFF_BAR + kWarps * kStages * 8;
+  static constexpr int RED_BYTES = kWarps * 16 * RANK * 4;
+  static constexpr int SMEM_BYTES = OFF_RED + RED_BYTES + 1024;     // + alignment slack
+};
+
+// RD(1/d) and RN((1 - RD(1/d) d) / d): the two-term reciprocal of d
+SVDQ_DEVINL float2 recip2(float d) {
+  const float hi = __frcp_rd(d);
+  return make_float2(hi, __fdiv_rn(__fmaf_rn(-hi, d, 1.0f), d));
+}
+
+// quantize one 16-element block held by one thread (8 bf16x2 words);
+// r6 = recip2(6), tab[code] = recip2(e4m3 value of code) (zeros for code 0)
+SVDQ_DEVINL void quant_block16(const uint32_t (&w)[8], const float (&inv)[16], float2 r6,
+                               const float2* tab, uint2& codes, uint32_t& sbyte) {
   float xh[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -50,187 +81,222 @@ SVDQ_DEVINL void quant_block16(const uint32_t (&w)[8], const float (&inv)[16], u
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(xh[i]));
-  sbyte = f32_to_e4m3_sat(__fdiv_rn(amax, 6.0f));
-  const float s = e4m3_to_f32(sbyte);
+  sbyte = f32_to_e4m3_sat(__fmaf_rn(amax, r6.x, __fmul_rn(amax, r6.y)));
+  const float2 r = tab[sbyte];
   float y[16];
-  if (s == 0.0f) {
-    codes = make_uint2(0u, 0u);
-    return;
-  }
-  if (!(amax <= 3.402823466e38f)) {  // infinite block: plain IEEE division
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = __fdiv_rn(xh[i], s);
-  } else {
-    const float r_hi = __frcp_rd(s);
-    const float r_lo = __fdiv_rn(__fmaf_rn(-r_hi, s, 1.0f), s);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = __fmaf_rn(xh[i], r_hi, __fmul_rn(xh[i], r_lo));
-  }
-  codes.x = f32x8_to_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
-  codes.y = f32x8_to_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+  for (int i = 0; i < 16; ++i) y[i] = __fmaf_rn(xh[i], r.x, __fmul_rn(xh[i], r.y));
+  const uint32_t keep = sbyte ? 0xFFFFFFFFu : 0u;  // scale 0: every code +0
+  codes.x = f32x8_to_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]) & keep;
+  codes.y = f32x8_to_e2m1x8(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]) & keep;
 }
 
-SVDQ_DEVINL void unpack8(const uint4& a, const uint4& b, uint32_t (&w)[8]) {
-  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+SVDQ_DEVINL float4 lds128f(const uint8_t* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
 }
 
-template <int RANK, int MT>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_quantize_act(const uint16_t* __restrict__ X, const float* __restrict__ inv_lambda,
-                   const uint16_t* __restrict__ L1s, int M, int K,
+// 16 bf16 of row `row` of a 128-byte-swizzled tile, chunks 2t and 2t+1
+SVDQ_DEVINL void load_row16(const uint8_t* tile, int row, int t, uint32_t (&w)[8]) {
+  const int sw = row & 7;
+  const uint4 lo = lds128(tile + row * 128 + (((2 * t) ^ sw) << 4));
+  const uint4 hi = lds128(tile + row * 128 + (((2 * t + 1) ^ sw) << 4));
+  w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+  w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+}
+
+// L1s rows g + 8n, k0 .. k0+15 (16 bf16 each): B fragments of NT n-tiles
+template <int NT>
+SVDQ_DEVINL void load_l1s(const uint16_t* __restrict__ L1s, int K, int g, int k0,
+                          uint32_t (&b)[NT][8]) {
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const uint16_t* p = L1s + (size_t)(g + 8 * n) * K + k0;
+    const uint4 lo = ld_keep_v4(p), hi = ld_keep_v4(p + 8);
+    b[n][0] = lo.x; b[n][1] = lo.y; b[n][2] = lo.z; b[n][3] = lo.w;
+    b[n][4] = hi.x; b[n][5] = hi.y; b[n][6] = hi.z; b[n][7] = hi.w;
+  }
+}
+
+template <int RANK>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_quantize_act(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ L1s,
+                   const float* __restrict__ inv_lambda, int M, int K,
                    uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_scales,
-                   uint16_t* __restrict__ lora_act) {
-  constexpr int NT = RANK / 8;        // n8 tiles of the down projection
-  constexpr int ROWS = 16 * MT;       // rows of this CTA
-  constexpr int NR = 2 * MT;          // rows per thread: g, g+8, g+16, g+24
-  extern __shared__ float red[];      // [kWarps][ROWS][RANK]
+                   uint16_t* __restrict__ lora_act, int* dev_status, uint64_t wait_ns) {
+  using C = QCfg<RANK>;
+  constexpr int NT = C::NT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int m0 = blockIdx.x * ROWS;
+  const int m0 = blockIdx.x * 16;
   const int steps = K >> 6;
-  const int s_begin = (warp * steps) / kWarps, s_end = ((warp + 1) * steps) / kWarps;
-  const size_t rowpitch = (size_t)K;   // bf16 elements
-  const int C4 = K >> 6;               // 4-column scale groups per row
+  const int s_begin = (warp * steps) / kWarps;
+  const int nst = ((warp + 1) * steps) / kWarps - s_begin;
+  uint8_t* xring = smem + C::OFF_X + warp * kStages * C::X_BYTES;
+  uint8_t* iring = smem + C::OFF_INV + warp * kStages * C::INV_BYTES;
+  float2* tab = reinterpret_cast<float2*>(smem + C::OFF_TAB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * kStages;
+  const int C4 = K >> 6;  // 4-column scale groups per row
+  const int rowA = m0 + g, rowB = m0 + g + 8;
+  const bool okA = rowA < M, okB = rowB < M;
 
-  int rows[NR];
-  bool ok[NR];
-#pragma unroll
-  for (int j = 0; j < NR; ++j) {
-    rows[j] = m0 + g + 8 * j;
-    ok[j] = rows[j] < M;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_x);
   }
+  __syncwarp();
+  int issued = 0;  // lane 0 only
+  auto issue = [&](int i) {
+    const int slot = i % kStages;
+    const int k0 = (s_begin + i) * 64;
+    mbar_arrive_expect_tx(&bars[slot], (uint32_t)C::TX_BYTES);
+    tma_load_2d(xring + slot * C::X_BYTES, &tm_x, &bars[slot], k0, m0);
+    bulk_load(iring + slot * C::INV_BYTES, inv_lambda + k0, (uint32_t)C::INV_BYTES, &bars[slot]);
+  };
+  if (lane == 0)
+    for (; issued < min(kStages, nst); ++issued) issue(issued);
 
-  float acc[MT][NT][4];
-#pragma unroll
-  for (int a = 0; a < MT; ++a)
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[a][n][c] = 0.0f;
+  // two-term reciprocals of the 127 positive e4m3 values (code 0: zeros)
+  if (threadIdx.x < 128)
+    tab[threadIdx.x] = threadIdx.x == 0 || threadIdx.x == 127
+                           ? make_float2(0.0f, 0.0f)
+                           : recip2(e4m3_to_f32(threadIdx.x));
+  const float2 r6 = recip2(6.0f);
+  __syncthreads();
 
-  for (int st = s_begin; st < s_end; ++st) {
-    const int k0 = st * 64 + 16 * t;
-    // ---- loads: X (read once), inv_lambda and L1s (shared by all CTAs)
-    uint32_t xw[NR][8];
+  float acc[NT][4];
 #pragma unroll
-    for (int j = 0; j < NR; ++j) {
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (ok[j]) {
-        const uint16_t* p = X + (size_t)rows[j] * rowpitch + k0;
-        lo = ld_stream_v4(p);
-        hi = ld_stream_v4(p + 8);
-      }
-      unpack8(lo, hi, xw[j]);
-    }
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[n][c] = 0.0f;
+  uint32_t bfr[NT][8];
+  if (nst > 0) load_l1s<NT>(L1s, K, g, s_begin * 64 + 16 * t, bfr);
+
+  int consumed = 0;
+  for (int i = 0; i < nst; ++i) {
+    const int slot = i % kStages;
+    const int step = s_begin + i;
+    const int k0 = step * 64 + 16 * t;
+    const bool ok = mbar_wait(&bars[slot], (uint32_t)(i / kStages) & 1u, dev_status, wait_ns);
+    if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform abort on timeout
+    const uint8_t* xt = xring + slot * C::X_BYTES;
+    uint32_t xa[8], xb[8];
+    load_row16(xt, g, t, xa);
+    load_row16(xt, g + 8, t, xb);
     float inv[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 v = ld_keep_f4(inv_lambda + k0 + 4 * q);
+      const float4 v = lds128f(iring + slot * C::INV_BYTES + 64 * t + 16 * q);
       inv[4 * q] = v.x; inv[4 * q + 1] = v.y; inv[4 * q + 2] = v.z; inv[4 * q + 3] = v.w;
     }
-    uint32_t bw[NT][8];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const uint16_t* p = L1s + (size_t)(g + 8 * n) * K + k0;
-      unpack8(ld_keep_v4(p), ld_keep_v4(p + 8), bw[n]);
+    __syncwarp();
+    consumed = i + 1;
+    if (lane == 0 && issued < nst) {  // refill this slot: the warp has read it
+      fence_proxy_async_smem();
+      issue(issued);
+      ++issued;
     }
-    // ---- down projection: 4 k16 sub-steps x NT n-tiles x MT m-tiles
+    // ---- down projection: 4 k16 sub-steps x NT n-tiles
 #pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4)
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int a = 0; a < MT; ++a)
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-          mma_bf16_16816(acc[a][n], xw[2 * a][2 * j4], xw[2 * a + 1][2 * j4],
-                         xw[2 * a][2 * j4 + 1], xw[2 * a + 1][2 * j4 + 1], bw[n][2 * j4],
-                         bw[n][2 * j4 + 1]);
+      for (int j4 = 0; j4 < 4; ++j4)
+        mma_bf16_16816(acc[n], xa[2 * j4], xb[2 * j4], xa[2 * j4 + 1], xb[2 * j4 + 1],
+                       bfr[n][2 * j4], bfr[n][2 * j4 + 1]);
+    // the next step's L1s fragments: their L2 latency overlaps this step's
+    // quantization and the next tile's wait
+    if (i + 1 < nst) load_l1s<NT>(L1s, K, g, k0 + 64, bfr);
     // ---- quantization: one block per row
-    uint32_t sw[NR];
-#pragma unroll
-    for (int j = 0; j < NR; ++j) {
-      uint2 codes;
-      uint32_t sb;
-      quant_block16(xw[j], inv, codes, sb);
-      if (ok[j])
-        *reinterpret_cast<uint2*>(a_codes + (size_t)rows[j] * (K >> 1) + (k0 >> 1)) = codes;
-      // gather the 4 scale bytes of this row's 64-wide step across the quad
-      uint32_t word = sb << (8 * t);
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 1);
-      word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-      sw[j] = word;
-    }
-    // lane t of the quad writes the scale word of row j == t (tile layout:
+    uint2 ca, cb;
+    uint32_t sa, sb;
+    quant_block16(xa, inv, r6, tab, ca, sa);
+    quant_block16(xb, inv, r6, tab, cb, sb);
+    if (okA) *reinterpret_cast<uint2*>(a_codes + (size_t)rowA * (K >> 1) + (k0 >> 1)) = ca;
+    if (okB) *reinterpret_cast<uint2*>(a_codes + (size_t)rowB * (K >> 1) + (k0 >> 1)) = cb;
+    // gather the 4 scale bytes of each row's 64-wide step across the quad;
+    // lane t = 0 writes row g's word, lane t = 1 row g+8's (tile layout:
     // tile (r/128, c/4) of 512 bytes; entry (r%32)*16 + ((r/32)%4)*4 + c%4)
-#pragma unroll
-    for (int j = 0; j < NR; ++j) {
-      if (j == t && ok[j]) {
-        const int r = rows[j];
-        const size_t off = ((size_t)(r >> 7) * C4 + st) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-        *reinterpret_cast<uint32_t*>(a_scales + off) = sw[j];
+    uint32_t wa = sa << (8 * t), wb = sb << (8 * t);
+    wa |= __shfl_xor_sync(0xFFFFFFFFu, wa, 1);
+    wa |= __shfl_xor_sync(0xFFFFFFFFu, wa, 2);
+    wb |= __shfl_xor_sync(0xFFFFFFFFu, wb, 1);
+    wb |= __shfl_xor_sync(0xFFFFFFFFu, wb, 2);
+    if (t < 2) {
+      const int r = t == 0 ? rowA : rowB;
+      if (r < M) {
+        const size_t off =
+            ((size_t)(r >> 7) * C4 + step) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+        *reinterpret_cast<uint32_t*>(a_scales + off) = t == 0 ? wa : wb;
       }
     }
   }
+  if (lane == 0 && consumed < nst) {
+    // timed out: let every copy already issued land before the CTA exits
+    for (int i = consumed; i < issued; ++i)
+      mbar_wait(&bars[i % kStages], (uint32_t)(i / kStages) & 1u, nullptr, wait_ns);
+  }
 
   // ---- reduce the warps' partial lora sums in a fixed order, round once
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 #pragma unroll
-  for (int a = 0; a < MT; ++a)
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int col = 8 * n + 2 * t;
-      float* base = red + ((size_t)warp * ROWS + 16 * a + g) * RANK + col;
-      base[0] = acc[a][n][0];
-      base[1] = acc[a][n][1];
-      base[8 * RANK] = acc[a][n][2];
-      base[8 * RANK + 1] = acc[a][n][3];
-    }
+  for (int n = 0; n < NT; ++n) {
+    const int col = 8 * n + 2 * t;
+    float* base = red + ((size_t)warp * 16 + g) * RANK + col;
+    base[0] = acc[n][0];
+    base[1] = acc[n][1];
+    base[8 * RANK] = acc[n][2];
+    base[8 * RANK + 1] = acc[n][3];
+  }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < ROWS * RANK; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < 16 * RANK; idx += kThreads) {
     float s = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += red[(size_t)w * ROWS * RANK + idx];
+    for (int w = 0; w < kWarps; ++w) s += red[(size_t)w * 16 * RANK + idx];
     const int r = m0 + idx / RANK;
     if (r < M) lora_act[(size_t)m0 * RANK + idx] = f32_to_bf16_rn(s);
   }
 }
 
-template <int RANK, int MT>
-cudaError_t launch_t(const uint16_t* X, const float* inv_lambda, const uint16_t* L1s, int M,
-                     int K, uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
-                     cudaStream_t stream) {
-  constexpr int ROWS = 16 * MT;
-  const size_t smem = (size_t)kWarps * ROWS * RANK * sizeof(float);
-  auto kern = k_quantize_act<RANK, MT>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  const int grid = (M + ROWS - 1) / ROWS;
-  kern<<<grid, kThreads, smem, stream>>>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act);
+template <int RANK>
+cudaError_t launch_t(const CUtensorMap& tm_x, const uint16_t* L1s, const float* inv_lambda,
+                     int M, int K, uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
+                     int* dev_status, cudaStream_t stream) {
+  using C = QCfg<RANK>;
+  auto kern = k_quantize_act<RANK>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = (M + 15) / 16;
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_x, L1s, inv_lambda, M, K, a_codes,
+                                                   a_scales, lora_act, dev_status,
+                                                   kWaitTimeoutNs);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_quantize_act(const uint16_t* X, const float* inv_lambda, const uint16_t* L1s,
-                                int M, int K, int rank, uint8_t* a_codes, uint8_t* a_scales,
-                                uint16_t* lora_act, int* /*dev_status*/, cudaStream_t stream,
-                                int num_sms) {
-  // two m16 tiles per warp halve the L1s traffic when there are enough rows
-  // to keep every SM busy; otherwise one tile per warp
-  const bool wide = (M + 31) / 32 >= num_sms;
+cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const uint16_t* L1s,
+                                const float* inv_lambda, int M, int K, int rank,
+                                uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
+                                int* dev_status, cudaStream_t stream) {
   switch (rank) {
     case 16:
-      return wide ? launch_t<16, 2>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream)
-                  : launch_t<16, 1>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream);
+      return launch_t<16>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
+                          stream);
     case 32:
-      return wide ? launch_t<32, 2>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream)
-                  : launch_t<32, 1>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream);
+      return launch_t<32>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
+                          stream);
     case 64:
-      return wide ? launch_t<64, 2>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream)
-                  : launch_t<64, 1>(X, inv_lambda, L1s, M, K, a_codes, a_scales, lora_act, stream);
+      return launch_t<64>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
+                          stream);
     default:
       return cudaErrorInvalidValue;
   }

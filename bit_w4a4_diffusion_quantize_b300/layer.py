@@ -25,7 +25,7 @@ class SVDQLinear:
 
         self.inv_lambda = t(packed["inv_lambda"].astype(np.float32), torch.float32)
         self.L1s = t(packed["L1s"].astype(np.uint16).view(np.int16), torch.bfloat16)
-        self.L2 = t(packed["L2"].astype(np.uint16).view(np.int16), torch.bfloat16)
+        self.L2s = t(packed["L2s"].astype(np.uint16).view(np.int16), torch.bfloat16)
         self.w_codes = t(packed["w_codes"].astype(np.uint8), torch.uint8)
         self.w_scales = t(packed["w_scales"].astype(np.uint8), torch.uint8)
         self.w_tensor_scale = float(packed["w_tensor_scale"])
@@ -46,7 +46,7 @@ class SVDQLinear:
             X, self.inv_lambda, self.L1s, self.rank, *bufs, dev_status=dev_status,
             stream=stream)
         return _lib.svdq_gemm_w4a4(a_codes, a_scales, self.w_codes, self.w_scales,
-                                   self.w_tensor_scale, lora, self.L2, self.bias, M, self.N,
+                                   self.w_tensor_scale, lora, self.L2s, self.bias, M, self.N,
                                    self.K, self.rank, Y=out, dev_status=dev_status,
                                    stream=stream)
 

@@ -59,8 +59,15 @@
  *            (SVDQ_SCALE_BYTES(rows, K)); padding rows are neither written
  *            nor used.  This is the order in which the tensor core reads
  *            block scales, so the GEMM copies them without reshuffling.
- *   lora     [M][rank] bf16 row-major;  L1s [K][rank] bf16;  L2 [rank][N]
- *            bf16;  Y [M][N] bf16;  bias [N] bf16.
+ *   lora     [M][rank] bf16 row-major (lora_act).
+ *   L1s      [rank][K] bf16: the K x rank down-projection factor stored
+ *            transposed (row i = column i of L1s, k contiguous).
+ *   L2s      [N][rank] bf16: the rank x N up-projection factor transposed
+ *            and divided by the weight tensor scale, L2s[n][i] = L2[i][n] / s_T
+ *            (exact for a power-of-two s_T unless the quotient leaves the bf16
+ *            normal range), so that the tensor cores can add the rank-r term
+ *            into the same accumulator as the 4-bit product.
+ *   Y [M][N] bf16;  bias [N] bf16.
  */
 #ifndef SVDQ_H_
 #define SVDQ_H_
@@ -120,24 +127,26 @@ svdq_status svdq_calib_absmax(const uint16_t* X_bf16, int64_t M, int64_t K,
  *   L1 L2      = rank-r truncated SVD of W_hat^T (L1 = U_r S_r, L2 = V_r^T),
  *                by randomized subspace iteration with a Jacobi SVD of the
  *                projected matrix (full Jacobi SVD when min(K, N) is small)
- *   L1s        = bf16(inv_lambda[k] * L1[k][i])   -> out [K][rank]
- *   L2         = bf16(L2)                          -> out [rank][N]
- *   R[k][n]    = (W[n][k] - sum_{i ascending} L1s[k][i] L2[i][n]) / inv_lambda[k]
+ *   L1s        = bf16(inv_lambda[k] * L1[k][i])   -> out [rank][K] (transposed)
+ *   L2b        = bf16(L2)
+ *   R[k][n]    = (W[n][k] - sum_{i ascending} L1s[k][i] L2b[i][n]) / inv_lambda[k]
  *                (float64, one rounding per operation, no fused multiply-add)
- *   s_T        = smallest power of two with 6*448*s_T >= max|R| (1 if R == 0)
+ *   s_T        = smallest power of two with 6*448*s_T >= max|R| (1 if R == 0),
+ *                within [2^-100, 2^100] (SVDQ_ERR_VALUE otherwise)
+ *   L2s        = L2b^T / s_T (exact)                 -> out [N][rank]
  *   w_scales   = RNE_e4m3(amax16 / (6 s_T)) per 16 consecutive k of each
  *                output channel n, in the scale tile layout (rows = N)
  *   w_codes    = RNE_e2m1(R[k][n] / (s_b s_T)), [N][K/2] packed
  *
  * Sizes: N % 128 == 0, K % 128 == 0, 1 <= rank <= min(K, N).  Buffers:
- * inv_lambda [K], L1s [K*rank], L2 [rank*N], w_codes SVDQ_CODE_BYTES(N, K),
+ * inv_lambda [K], L1s [rank*K], L2s [N*rank], w_codes SVDQ_CODE_BYTES(N, K),
  * w_scales SVDQ_SCALE_BYTES(N, K), w_tensor_scale [1].
  * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_VALUE
  * (non-finite W or x_absmax, or a residual beyond the float range),
  * SVDQ_ERR_NOMEM. */
 svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absmax,
                               int rank, float* inv_lambda, uint16_t* L1s,
-                              uint16_t* L2, uint8_t* w_codes, uint8_t* w_scales,
+                              uint16_t* L2s, uint8_t* w_codes, uint8_t* w_scales,
                               float* w_tensor_scale);
 
 /* Offline packing of a modulation-layer weight W [N][K] (fp32, host) to AWQ
@@ -164,7 +173,7 @@ svdq_status awq_pack_weights(const float* W, int N, int K, int group_size,
  *   x_hat          = fl32(X[m][k] * inv_lambda[k])
  *   a_scales       = RNE_e4m3(amax16(x_hat) / 6)   (scale tile layout, rows = M)
  *   a_codes        = RNE_e2m1(x_hat / s)           ([M][K/2] packed)
- * Inputs: X [M][K] bf16, inv_lambda [K] fp32, L1s [K][rank] bf16.
+ * Inputs: X [M][K] bf16, inv_lambda [K] fp32, L1s [rank][K] bf16.
  * Outputs: a_codes SVDQ_CODE_BYTES(M, K), a_scales SVDQ_SCALE_BYTES(M, K),
  * lora_act [M][rank] bf16.
  * Sizes: M >= 0 (M == 0 launches nothing), K % 128 == 0, rank in {16, 32, 64}.
@@ -179,12 +188,12 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
  * epilogue (fused-kernel paragraph: up projection fused with the 4-bit
  * compute kernel):
  *   Y = bf16( s_T * sum_k dec(a)[m][k] dec(w)[n][k]
- *             + sum_i lora_act[m][i] L2[i][n] + bias[n] )
+ *             + sum_i lora_act[m][i] L2s[n][i] * s_T + bias[n] )
  * dec(.) = e2m1 value x e4m3 block scale.  tcgen05 block-scaled NVFP4 MMA
  * with fp32 accumulators in tensor memory; operands and scales staged by TMA.
  * The rank-r term is accumulated on the tensor cores into the same fp32
- * accumulator as bf16(L2[i][n] / s_T), which is exact because s_T must be a
- * power of two (as svdq_pack_weights produces).
+ * accumulator (L2s already carries 1/s_T; s_T must be a power of two, as
+ * svdq_pack_weights produces).  Persistent kernel, one CTA per SM.
  * Inputs: activation side as written by svdq_quantize_act (rows = M), weight
  * side as written by svdq_pack_weights (rows = N), bias nullable.
  * Output: Y [M][N] bf16.
@@ -196,7 +205,7 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
 svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
                            const uint8_t* w_codes, const uint8_t* w_scales,
                            float w_tensor_scale, const uint16_t* lora_act,
-                           const uint16_t* L2, const uint16_t* bias, uint16_t* Y,
+                           const uint16_t* L2s, const uint16_t* bias, uint16_t* Y,
                            int M, int N, int K, int rank, int* dev_status,
                            void* stream);
 
@@ -206,7 +215,8 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
  * fp32 accumulation.  Streams the 4-bit weights once from HBM.
  * Inputs: X [M][K] bf16; qweight [N][K/2] (even k in the low nibble);
  * scales, zeros [N][K/64] fp16; bias [N] bf16 (nullable).  Output Y [M][N] bf16.
- * Sizes: 1 <= M <= 8, N >= 1, K % 128 == 0, group_size == 64.
+ * Sizes: 1 <= M <= 8, N % 8 == 0 (N >= 8), K % 128 == 0, K <= 4096 (X and
+ * its per-group sums are staged in shared memory), group_size == 64.
  * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_ALIGN,
  * SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA. */
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

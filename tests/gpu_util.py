@@ -70,7 +70,8 @@ def oracle_weight_operands(packed: dict, bias_values=None) -> dict:
     out = {
         "inv_lambda": dev_f32(packed["inv_lambda"]),
         "L1s": dev_bits16(formats.bf16_bits(packed["L1s"]).T.copy()),     # [r][K]
-        "L2": dev_bits16(formats.bf16_bits(packed["L2"])),                 # [r][N]
+        # [N][r], divided by the power-of-two tensor scale (exact)
+        "L2": dev_bits16(formats.bf16_bits(packed["L2"].T / packed["s_T"])),
         "w_codes": dev_u8(packed["w_codes_packed"]),
         "w_scales": dev_u8(packed["w_scales_swizzled"]),
         "s_T": float(packed["s_T"]),

@@ -93,8 +93,8 @@ def test_gemm_exact_operands_reproduce_plain_product():
     from oracle import layout
     Y = lib.svdq_gemm_w4a4(dev_u8(layout.pack_nibbles(a_codes)), dev_u8(layout.sf_swizzle(a_sc)),
                            dev_u8(layout.pack_nibbles(w_codes)), dev_u8(layout.sf_swizzle(w_sc)),
-                           s_T, dev_bf16(lora.astype(np.float32)), dev_bf16(L2.astype(np.float32)),
-                           None, M, N, K, 16)
+                           s_T, dev_bf16(lora.astype(np.float32)),
+                           dev_bf16(L2.T.copy().astype(np.float32)), None, M, N, K, 16)
     torch.cuda.synchronize()
     y = host_bf16(Y)
     # exact products of few-bit values: fp32 accumulation is exact here too

@@ -1,7 +1,8 @@
 """svdq_quantize_act on the GPU against the oracle: e4m3 scales and e2m1
-codes bit-exact, lora_act within one bf16 ulp of the oracle's rounded exact
-sum (fp32 tensor-core accumulation may flip a rounding that sits within
-~1e-6 relative of a bf16 midpoint)."""
+codes bit-exact; lora_act within one bf16 ulp of the oracle's rounded exact
+sum plus the fp32 accumulation allowance 2^-20 * sum_k |x_k L1s[k,i]| (the
+tensor cores accumulate in fp32 in their own order; where the sum cancels,
+that error is measured against the size of the terms, not of the result)."""
 import numpy as np
 import pytest
 import torch
@@ -37,7 +38,9 @@ def _check(X, inv, L1s, rank, lora_rows=None):
     l_ref = svdq.lora_down(X[rows], L1s)
     diff = np.abs(lora[rows] - l_ref)
     ulp = 2 * np.maximum(np.ldexp(1.0, np.frexp(np.abs(l_ref))[1] - 9), 2.0 ** -133)
-    assert np.all(diff <= ulp), f"lora differs by more than 1 ulp: {np.max(diff / ulp):.2f} ulp"
+    mag = np.abs(X[rows].astype(np.float64)) @ np.abs(L1s)
+    allow = ulp + 2.0 ** -20 * mag
+    assert np.all(diff <= allow), f"lora error {np.max(diff / allow):.2f} x the allowance"
     return np.mean(diff > 0)
 
 
@@ -122,8 +125,8 @@ def test_quantize_act_special_values():
     X[7, :] = workloads.to_bf16_values(X[7] * np.float32(1e-20))    # underflowing block scale
     inv = (rng.uniform(0.3, 3.0, K)).astype(np.float32)
     L1s = formats.round_to_bf16(rng.standard_normal((K, 32)) * 0.05)
-    finite_rows = np.where(np.all(np.isfinite(X * inv), axis=1))[0]
     with np.errstate(over="ignore", invalid="ignore"):
+        finite_rows = np.where(np.all(np.isfinite(X * inv), axis=1))[0]
         _check(X, inv, L1s, 32, lora_rows=finite_rows)
 
 
@@ -139,5 +142,6 @@ def test_quantize_act_repeatable():
     a = _run(X, inv, L1s, 32)
     b = _run(X, inv, L1s, 32)
     assert np.array_equal(a[0], b[0])
-    assert np.array_equal(a[1].cpu().numpy(), b[1].cpu().numpy())
+    # padding rows of the scale tiles are never written: compare the real rows
+    assert np.array_equal(scales_from_device(a[1], 200, 512), scales_from_device(b[1], 200, 512))
     assert np.array_equal(a[2], b[2])

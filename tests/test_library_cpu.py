@@ -97,7 +97,7 @@ def test_gemm_argument_errors():
 
 def test_awq_argument_errors():
     assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(K=192) == -2 and _awq(g=128) == -2
-    assert _awq(N=0) == -2
+    assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
     assert _awq(X=P(0)) == -1 and _awq(X=MISALIGNED) == -3
 
 
@@ -134,7 +134,7 @@ def test_packer_matches_oracle(case):
     # factors are bf16; the residual of the packer's own factors, quantized by
     # the oracle, must equal the packer's codes, scales and tensor scale
     L1s = formats.bf16_from_bits(p["L1s"]).T
-    L2 = formats.bf16_from_bits(p["L2"])
+    L2 = formats.bf16_from_bits(p["L2s"]).T * p["w_tensor_scale"]
     R = svdq.residual(W, p["inv_lambda"], L1s, L2)
     sT = svdq.tensor_scale(R)
     codes, sc = svdq.quantize_weight_residual(R, sT)
@@ -152,7 +152,7 @@ def test_packer_full_rank_leaves_rounding_residual():
                                  planted_rank=8)
     X, W, xm, p = _packer_case(case)
     L1s = formats.bf16_from_bits(p["L1s"]).T
-    L2 = formats.bf16_from_bits(p["L2"])
+    L2 = formats.bf16_from_bits(p["L2s"]).T * p["w_tensor_scale"]
     W_hat = W.T.astype(np.float64) / p["inv_lambda"].astype(np.float64)[:, None]
     R = svdq.residual(W, p["inv_lambda"], L1s, L2)
     # only the bf16 rounding of the factors is left
