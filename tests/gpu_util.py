@@ -5,7 +5,16 @@ Output tolerance (float outputs): the device rounds Y once to bf16 and
 accumulates in fp32 on tensor cores; the oracle returns Y unrounded in fp64.
 Relative Frobenius error <= 2e-3, and elementwise
 |Y_dev - Y_ref| <= 1e-2 * rms(Y_ref) + ulp_bf16(Y_ref)/2 (the half-ulp term
-covers the final bf16 rounding of large outputs)."""
+covers the final bf16 rounding of large outputs) + the lora rounding slack.
+
+Lora rounding slack: lora_act is stored in bf16 by both sides, rounded from
+the exact sum by the oracle and from an fp32 tensor-core sum by the device.
+Where the exact sum lies within the fp32 accumulation allowance
+2^-20 * sum_k |x_k L1s[k,i]| of a bf16 rounding boundary, either neighbour is a
+correct result, and the two choices differ in Y by |delta lora_i| * |L2[i,n]|
+(up to 0.15 at the diffusion-transformer scales: |lora| reaches 512, where one
+bf16 step is 4).  The slack adds that difference for exactly those (row, i)
+pairs; it is computed from the oracle's values alone."""
 from __future__ import annotations
 
 import numpy as np
@@ -48,7 +57,23 @@ def half_ulp_bf16(y: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, e - 9)  # ulp = 2^(e-1-7); half of it
 
 
-def assert_y_close(y_dev: np.ndarray, y_ref: np.ndarray, what: str = "Y"):
+def lora_rounding_slack(X: np.ndarray, L1s: np.ndarray, L2: np.ndarray):
+    """(rows, slack[len(rows), N]): the Y slack of the rows that hold an
+    ambiguous lora_act rounding (see the module docstring)."""
+    X = np.asarray(X, dtype=np.float64)
+    L1s = np.asarray(L1s, dtype=np.float64)
+    exact = X @ L1s
+    ref = formats.round_to_bf16(exact)
+    allow = 2.0 ** -20 * (np.abs(X) @ np.abs(L1s))
+    amb = np.maximum(np.abs(formats.round_to_bf16(exact + allow) - ref),
+                     np.abs(formats.round_to_bf16(exact - allow) - ref))
+    rows = np.nonzero(np.any(amb > 0, axis=1))[0]
+    return rows, amb[rows] @ np.abs(np.asarray(L2, dtype=np.float64))
+
+
+def assert_y_close(y_dev: np.ndarray, y_ref: np.ndarray, what: str = "Y", slack=None):
+    """slack: None or (rows, extra[len(rows), N]) added to the elementwise
+    bound of those rows (lora_rounding_slack)."""
     y_dev = np.asarray(y_dev, dtype=np.float64)
     y_ref = np.asarray(y_ref, dtype=np.float64)
     assert y_dev.shape == y_ref.shape
@@ -57,6 +82,8 @@ def assert_y_close(y_dev: np.ndarray, y_ref: np.ndarray, what: str = "Y"):
     rel = np.linalg.norm(err) / max(np.linalg.norm(y_ref), 1e-300)
     rms = np.sqrt(np.mean(y_ref ** 2)) if y_ref.size else 0.0
     bound = ABS_RMS_TOL * rms + half_ulp_bf16(y_ref)
+    if slack is not None and len(slack[0]):
+        bound[slack[0]] += slack[1]
     worst = np.max(np.abs(err) - bound) if err.size else -1.0
     assert rel <= REL_FRO_TOL, f"{what}: relative Frobenius error {rel:.3e} > {REL_FRO_TOL}"
     assert worst <= 0, (f"{what}: elementwise error exceeds 1e-2*rms + ulp/2 by {worst:.3e} "
