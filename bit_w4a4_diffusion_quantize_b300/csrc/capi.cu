@@ -106,11 +106,11 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][K/2] bytes of 4-bit codes: box 64 bytes (128 codes) x box_rows,
-// 64B swizzle (the GEMM's K-major operand tiles)
+// [rows][K/2] bytes of 4-bit codes: box 128 bytes (256 codes) x box_rows,
+// 128B swizzle (the GEMM's K-major operand tiles)
 bool encode_codes(CUtensorMap* map, const uint8_t* ptr, int rows, int K, int box_rows) {
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, (uint64_t)K / 2, (uint64_t)rows,
-                   (uint64_t)K / 2, 64u, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
+                   (uint64_t)K / 2, 128u, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // [rows][rank] bf16 rank-r operand: one row per box line, swizzle span = row bytes
@@ -195,18 +195,16 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
   const int block_n = (N % 256 == 0) ? 256 : 128;
   svdq::GemmMaps maps;
   if (!encode_codes(&maps.a_codes, a_codes, M, K, 128) ||
-      !encode_codes(&maps.w_codes, w_codes, N, K, block_n) ||
+      !encode_codes(&maps.w_codes, w_codes, N, K, block_n / 2) ||
       !encode_rank_rows(&maps.lora, lora_act, M, rank, 128) ||
-      !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n) ||
-      !encode_2d(&maps.y, CU_TENSOR_MAP_DATA_TYPE_UINT16, Y, (uint64_t)N, (uint64_t)M,
-                 (uint64_t)N * 2, 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n))
     return SVDQ_ERR_CUDA;
   // test hook: SVDQ_TEST_GEMM_STALL=1 makes the kernel's loader issue nothing
   // so that its pipeline wait times out after 100 ms (status SVDQ_DEV_TIMEOUT)
   const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
   const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
-                                         bias, M, N, K, rank, dev_status, test_stall, sms,
+                                         bias, Y, M, N, K, rank, dev_status, test_stall, sms,
                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }

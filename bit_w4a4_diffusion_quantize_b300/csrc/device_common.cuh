@@ -191,6 +191,37 @@ SVDQ_DEVINL void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uin
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// The same loads, delivered to the same shared-memory offset (and completing
+// on the mbarrier at the same offset) in every CTA of the cluster in `mask`.
+SVDQ_DEVINL void tma_load_2d_mc(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y,
+                                uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+SVDQ_DEVINL void bulk_load_mc(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                              uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+// ---------------------------------------------------------------- clusters
+SVDQ_DEVINL uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster (release/acquire)
+SVDQ_DEVINL void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
 // 2-D tiled TMA store of a shared-memory box to global memory (bulk group)
 SVDQ_DEVINL void tma_store_2d(const void* tmap, const void* smem_src, int x, int y) {
   asm volatile(
@@ -240,6 +271,15 @@ SVDQ_DEVINL void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+// the same commit, arriving once on the mbarrier at this offset in every CTA
+// of the cluster in `mask`
+SVDQ_DEVINL void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
       : "memory");
 }
 // block-scaled NVFP4 MMA: D(tmem) (+)= A(smem) x B(smem), scales in TMEM

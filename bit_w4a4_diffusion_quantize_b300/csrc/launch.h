@@ -16,17 +16,16 @@ cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const uint16_t* L1s,
 
 // Tensor maps of svdq_gemm_w4a4.
 struct GemmMaps {
-  CUtensorMap a_codes;  // [M][K/2] bytes: box 64 x 128 rows, 64B swizzle
-  CUtensorMap w_codes;  // [N][K/2] bytes: box 64 x BN rows, 64B swizzle
+  CUtensorMap a_codes;  // [M][K/2] bytes: box 128 x 128 rows, 128B swizzle
+  CUtensorMap w_codes;  // [N][K/2] bytes: box 128 x BN/2 rows (one CTA's half), 128B swizzle
   CUtensorMap lora;     // lora_act [M][rank] bf16: box rank x 128 rows, swizzle = 2*rank bytes
   CUtensorMap l2s;      // L2s [N][rank] bf16: box rank x BN rows, same swizzle
-  CUtensorMap y;        // Y [M][N] bf16: box 64 x 32 rows, 128B swizzle (stores)
 };
 
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
-                             int M, int N, int K, int rank, int* dev_status, int test_stall,
-                             int num_sms, cudaStream_t stream);
+                             uint16_t* Y, int M, int N, int K, int rank, int* dev_status,
+                             int test_stall, int num_sms, cudaStream_t stream);
 
 // Largest K the AWQ GEMV stages in shared memory.
 int awq_max_k();
