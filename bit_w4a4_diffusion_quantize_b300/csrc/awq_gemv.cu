@@ -3,29 +3,37 @@
 // diffusion models", kernel-family list: awq_w4a16 serves the memory-bound
 // adaLN modulation projections; config block: int4, group_size 64).
 //
-//   Y[m][n] = bf16( sum_g s[n][g] * ( sum_{k in g} q[n][k] x[m][k]
-//                                     - z[n][g] * sum_{k in g} x[m][k] ) + bias[n] )
+//   Y[m][n] = bf16( sum_g s[n][g] * ( sum_{k in g} (128 + q[n][k]) x[m][k]
+//                                     - (128 + z[n][g]) * sum_{k in g} x[m][k] )
+//                   + bias[n] )
 //
 // which equals sum_k x (q - z) s.  The inner sums run on tensor cores
-// (m16n8k16, bf16 in, fp32 out) with the codes q as exact bf16 integers.  The
-// activations (M <= 8 rows, zero-padded to the MMA's 16) are the A operand
-// and stay in registers for the whole kernel: each warp owns a fixed range of
-// K groups; the weights are the B operand, 8 output channels per MMA.  Per
-// 64-group the fp32 partial sums get the scale and zero point;
-// sum_{k in g} x[m][k] is formed once per warp.
+// (m16n8k16, bf16 in, fp32 out).  The weights are the A operand: 16 rows of a
+// tile by 16 k per MMA, every code fed as the exact bf16 value 128 + q (a
+// nibble OR-ed into the mantissa of 128.0, 0x4300: one shift and one logic op
+// per pair of codes); the constant 128 is folded into the zero point.  The
+// activations (M <= 8 rows) are the B operand (N = 8 of the MMA, nothing
+// wasted) and stay in registers for the whole kernel: each of the 12 compute
+// warps of a CTA owns a fixed range of K groups.  Per 64-group the fp32 sums
+// get scale and zero point; sum_{k in g} x[m][k] is formed once per warp.
 //
-// Streaming.  The weights are read exactly once.  A persistent CTA walks its
-// 16-row tiles; one thread streams each tile (16 x K/2 bytes of codes as
-// 128-byte-wide TMA boxes with the 128-byte swizzle, plus the tile's fp16
-// scales and zeros as plain bulk copies) into a shared-memory ring of up to
-// 6 tiles.  The 8 warps split each tile's K groups; their fp32 partials are
-// added in a fixed order through shared memory.
+// Streaming.  The weights are read exactly once, by the compute warps
+// themselves: for each 16-row tile a lane copies the code words it feeds to
+// its MMAs (8 bytes of rows r and r + 8 per group; 4 lanes cover 32
+// contiguous bytes of a row, every sector is used whole), and its scale and
+// zero words, with per-thread asynchronous copies (cp.async) into its own
+// shared-memory slots, kStages tiles ahead of its math: enough bytes in flight
+// for HBM rate, no registers held, and no synchronisation beyond each lane
+// waiting for its own copies.  Scale and zero values reach the lanes that need
+// them through quad shuffles.  A persistent CTA walks tiles
+// blockIdx.x + j * gridDim.x.  The warps leave their fp32 partials in a ring
+// of reduction buffers (no CTA-wide barrier); a reduction warp adds the 12
+// partials and the bias in a fixed order and writes Y.
 //
-// The k order inside an MMA is permuted: a thread feeds 16 consecutive k of a
-// group, paired as (k, k+4) within each 8, the pairing in which two nibbles
-// of a 32-bit code word become one bf16x2 register: OR-ing a nibble into the
-// mantissa of 128.0 (0x4300) gives the bf16 value 128 + q exactly, and
-// subtracting 128 leaves q exactly.
+// The k order inside an MMA is permuted: a lane feeds 16 consecutive k of a
+// group (two 32-bit code words per weight row), paired as (k, k+4) within
+// each 8 -- the pairing in which two nibbles of a code word become one bf16x2
+// register -- and the activation fragments use the same permutation.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,18 +45,14 @@ namespace svdq {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kMaxStages = 6;
-constexpr int kGpw = 8;  // K groups per warp at most (K <= 8 * 8 * 64 = 4096)
-constexpr int kSmemBudget = 224 * 1024;
+constexpr int kCW = 12;                   // compute warps
+constexpr int kThreads = 32 * (kCW + 1);  // + the reduction warp
+constexpr int kRed = 4;  // reduction buffers (tiles whose partials may be in flight)
+constexpr int kStages = 4;  // tiles in flight per lane (cp.async groups)
 
-// nibbles at bit s and s+16 of w -> bf16x2 {q_lo, q_hi}
-SVDQ_DEVINL uint32_t nib2_to_bf16x2(uint32_t w, int s) {
-  const uint32_t v = ((w >> s) & 0x000F000Fu) | 0x43004300u;  // {128+q, 128+q'}
-  const __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v),
-                                   __floats2bfloat162_rn(128.0f, 128.0f));
-  return *reinterpret_cast<const uint32_t*>(&r);
+// nibbles at bit s and s+16 of w -> bf16x2 {128 + q_lo, 128 + q_hi} (exact)
+SVDQ_DEVINL uint32_t nib2_biased(uint32_t w, int s) {
+  return ((w >> s) & 0x000F000Fu) | 0x43004300u;
 }
 
 // bf16 element e (0..15) of the 8 words w
@@ -56,74 +60,117 @@ SVDQ_DEVINL uint32_t elem(const uint32_t (&w)[8], int e) {
   return (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
 }
 
-struct AwqLayout {
-  int G, boxes, code_bytes, sz_bytes, stage_bytes, stages, off_red, off_bar, smem;
-};
-
-__host__ __device__ inline AwqLayout awq_layout(int K) {
-  AwqLayout L;
-  L.G = K / 64;
-  L.boxes = (K / 2 + 127) / 128;       // 128-byte boxes per row
-  L.code_bytes = L.boxes * 16 * 128;   // 16 rows per tile
-  L.sz_bytes = 16 * L.G * 2;           // fp16 scales (and as much for zeros)
-  L.stage_bytes = (L.code_bytes + 2 * L.sz_bytes + 1023) / 1024 * 1024;
-  const int red = 2 * kWarps * 16 * 8 * 4;
-  int st = (kSmemBudget - red - 128 - 1024) / L.stage_bytes;
-  L.stages = st > kMaxStages ? kMaxStages : st;
-  L.off_red = L.stages * L.stage_bytes;
-  L.off_bar = L.off_red + red;
-  L.smem = L.off_bar + 128 + 1024;
-  return L;
+SVDQ_DEVINL uint32_t ld_stream_u16(const uint16_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
 }
 
+// shared-memory slots of one lane for one tile, 8 bytes each (lane-contiguous,
+// so every access is conflict-free): code words of rows r and r + 8 per group,
+// then the 4-byte words holding the scale and the zero of group t of rows r,
+// r + 8 (lanes t < groups; the fp16 value is the half picked by the index parity)
+template <int GPW>
+struct Slots {
+  static constexpr int kPerLane = 2 * GPW + 2;
+  static constexpr int kWarpStage = kPerLane * 32;  // uint2 per warp and stage
+};
+template <int GPW>
+constexpr int awq_smem_bytes() {
+  return kStages * kCW * Slots<GPW>::kWarpStage * 8;
+}
+
+#ifdef SVDQ_AWQ_TRACE
+// timeline instrumentation, compiled only into instrumented builds: the first
+// 8 CTAs stamp %globaltimer at fixed slots (512 per CTA)
+__device__ unsigned long long* g_awq_trace = nullptr;
+#define SVDQ_ATR(slot, idx)                                                          \
+  do {                                                                               \
+    if (g_awq_trace && blockIdx.x < 8 && (idx) < 32)                                 \
+      g_awq_trace[blockIdx.x * 512 + (slot) + (idx)] = globaltimer_ns();             \
+  } while (0)
+#else
+#define SVDQ_ATR(slot, idx) \
+  do {                      \
+  } while (0)
+#endif
+
+// GPW: K groups per compute warp at most (ceil(G / kCW), 1..6)
+template <int GPW>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_awq_gemv(const __grid_constant__ CUtensorMap tm_q, const uint16_t* __restrict__ X,
+    k_awq_gemv(const uint8_t* __restrict__ qw, const uint16_t* __restrict__ X,
                const uint16_t* __restrict__ sc, const uint16_t* __restrict__ zr,
                const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
                int* dev_status, uint64_t wait_ns) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const AwqLayout L = awq_layout(K);
-  const int G = L.G;
+  extern __shared__ uint2 slots[];  // [stage][warp][slot][lane]
+  __shared__ __align__(16) float red[kRed][kCW][16 * 8];  // [buffer][warp][row * 8 + m]
+  __shared__ __align__(8) uint64_t red_full[kRed];        // count kCW
+  __shared__ __align__(8) uint64_t red_empty[kRed];       // count 1
+  __shared__ volatile uint32_t abort_flag;
+  const int G = K / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2, t = lane & 3;  // MMA row (activation m / weight row), quad lane
-  float* red = reinterpret_cast<float*>(smem + L.off_red);  // [2][warps][16 rows][8 m]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
-  volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(smem + L.off_bar + 120);
+  const int r = lane >> 2, t = lane & 3;  // MMA group (weight row r / activation m) and quad lane
 
   const int tiles = (N + 15) >> 4;
   const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int stages = L.stages;
 
-  // ---- producer: one thread streams this CTA's tiles into the ring
-  auto issue = [&](int j) {
-    const int slot = j % stages;
-    const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-    uint8_t* st = smem + slot * L.stage_bytes;
-    const int rows = min(16, N - n0);
-    mbar_arrive_expect_tx(&full[slot], (uint32_t)(L.code_bytes + 2 * rows * G * 2));
-    for (int b = 0; b < L.boxes; ++b) tma_load_2d(st + b * 2048, &tm_q, &full[slot], b * 128, n0);
-    bulk_load(st + L.code_bytes, sc + (size_t)n0 * G, (uint32_t)(rows * G * 2), &full[slot]);
-    bulk_load(st + L.code_bytes + L.sz_bytes, zr + (size_t)n0 * G, (uint32_t)(rows * G * 2),
-              &full[slot]);
-  };
-  int issued = 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
-    *abort_flag = 0;
+    for (int b = 0; b < kRed; ++b) {
+      mbar_init(&red_full[b], kCW);
+      mbar_init(&red_empty[b], 1);
+    }
+    abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tm_q);
-    for (; issued < min(stages, my_tiles); ++issued) issue(issued);
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ---------------------------------------------------------- reduction warp
+    for (int j = 0; j < my_tiles; ++j) {
+      const int b = j % kRed;
+      const int n0 = (blockIdx.x + j * gridDim.x) * 16;
+      // the bias of tile j is fetched before its partials are waited for
+      uint32_t bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = (lane + 32 * i) >> 3;
+        bv[i] = (bias && n0 + row < N) ? ld_stream_u16(bias + n0 + row) : 0u;
+      }
+      const bool ok =
+          mbar_wait(&red_full[b], (uint32_t)(j / kRed) & 1u, dev_status, wait_ns) && !abort_flag;
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
+        abort_flag = 1;
+        break;
+      }
+      if (lane == 0) SVDQ_ATR(32, j);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int idx = lane + 32 * i, row = idx >> 3, m = idx & 7;
+        if (m < M && n0 + row < N) {
+          float s = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) s += red[b][w][idx];
+          s += __uint_as_float(bv[i] << 16);
+          Y[(size_t)m * N + n0 + row] = f32_to_bf16_rn(s);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[b]);
+      if (lane == 0) SVDQ_ATR(64, j);
+    }
+    return;
   }
 
-  // ---- this warp's activation fragments: groups [g_begin, g_end), row m = r,
-  // 16 consecutive k (16t .. 16t+15) paired (e, e+4) within each 8
-  const int g_begin = (warp * G) / kWarps, ng = ((warp + 1) * G) / kWarps - g_begin;
-  uint32_t afr[kGpw][8];
-  float sxr[kGpw];
+  // ---------------------------------------------------------------- compute warps
+  if (lane == 0 && warp == 0) SVDQ_ATR(1, 0);
+  // activation fragments of this warp's groups [g_begin, g_begin + ng): lane
+  // (r, t) holds x[m = r][64 g + 16 t .. + 15] as the B operand of the 4 MMAs
+  // of a group: MMA v takes k pairs (e, e + 4) and (e + 1, e + 5), e = 8 (v/2) + 2 (v%2)
+  const int g_begin = (warp * G) / kCW, ng = ((warp + 1) * G) / kCW - g_begin;
+  uint32_t bfr[GPW][8];
+  float sx[GPW][2];  // sum over the group's 64 k of x[m] for m = 2t, 2t + 1
 #pragma unroll
-  for (int gi = 0; gi < kGpw; ++gi) {
+  for (int gi = 0; gi < GPW; ++gi) {
     uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (gi < ng && r < M) {
       const uint16_t* xp = X + (size_t)r * K + (g_begin + gi) * 64 + 16 * t;
@@ -132,101 +179,141 @@ __global__ void __launch_bounds__(kThreads, 1)
       w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
     }
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const int e = 8 * (p >> 2) + (p & 3);
-      afr[gi][p] = elem(w, e) | (elem(w, e + 4) << 16);
+    for (int v = 0; v < 4; ++v) {
+      const int e = 8 * (v >> 1) + 2 * (v & 1);
+      bfr[gi][2 * v] = elem(w, e) | (elem(w, e + 4) << 16);
+      bfr[gi][2 * v + 1] = elem(w, e + 1) | (elem(w, e + 5) << 16);
     }
     float s = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) s += bf16lo_to_f32(w[i]) + bf16hi_to_f32(w[i]);
     s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-    sxr[gi] = s;  // sum over the group's 64 k of row m = r
+    s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);  // lanes of group r: sum for m = r
+    sx[gi][0] = __shfl_sync(0xFFFFFFFFu, s, 8 * t);      // m = 2t
+    sx[gi][1] = __shfl_sync(0xFFFFFFFFu, s, 8 * t + 4);  // m = 2t + 1
   }
-  __syncthreads();
+  if (lane == 0 && warp == 0) SVDQ_ATR(2, 0);
 
+  const size_t row_bytes = (size_t)K / 2;
+  constexpr int SL = Slots<GPW>::kPerLane;
+  // asynchronous copies of tile j into stage j % kStages (one commit group per
+  // tile, empty past the last tile, so that group counting stays uniform)
+  auto issue = [&](int j) {
+    if (j < my_tiles) {
+      const int n0 = (blockIdx.x + j * gridDim.x) * 16;
+      uint2* my = slots + ((size_t)((j % kStages) * kCW + warp) * SL) * 32 + lane;
+      const int lo_b = n0 + r < N ? 8 : 0, hi_b = n0 + r + 8 < N ? 8 : 0;
+      const uint8_t* q_lo = qw + (size_t)min(n0 + r, N - 1) * row_bytes + 8 * t;
+      const uint8_t* q_hi = qw + (size_t)min(n0 + r + 8, N - 1) * row_bytes + 8 * t;
+#pragma unroll
+      for (int gi = 0; gi < GPW; ++gi) {
+        if (gi < ng) {
+          const size_t off = (size_t)(g_begin + gi) * 32;
+          cp_async<8>(my + (2 * gi) * 32, q_lo + off, lo_b);
+          cp_async<8>(my + (2 * gi + 1) * 32, q_hi + off, hi_b);
+        }
+      }
+      if (t < ng) {
+        // the 4-byte word holding element i (i & ~1, i | 1): inside the array,
+        // whose element count N * G is even
+        const size_t i_lo = (size_t)min(n0 + r, N - 1) * G + g_begin + t;
+        const size_t i_hi = (size_t)min(n0 + r + 8, N - 1) * G + g_begin + t;
+        uint32_t* w = reinterpret_cast<uint32_t*>(my + (2 * GPW) * 32);
+        cp_async<4>(w, sc + (i_lo & ~(size_t)1), lo_b ? 4 : 0);
+        cp_async<4>(w + 1, sc + (i_hi & ~(size_t)1), hi_b ? 4 : 0);
+        cp_async<4>(w + 64, zr + (i_lo & ~(size_t)1), lo_b ? 4 : 0);
+        cp_async<4>(w + 65, zr + (i_hi & ~(size_t)1), hi_b ? 4 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int a = 0; a < kStages - 1; ++a) issue(a);
   for (int j = 0; j < my_tiles; ++j) {
-    const int slot = j % stages;
+    issue(j + kStages - 1);
+    cp_async_wait<kStages - 1>();  // this lane's copies of tile j have landed
     const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-    const bool ok = mbar_wait(&full[slot], (uint32_t)(j / stages) & 1u, dev_status, wait_ns);
-    if (!ok) *abort_flag = 1;
-    __syncthreads();
-    if (*abort_flag) break;  // CTA-uniform
-    const uint8_t* st = smem + slot * L.stage_bytes;
-    const uint16_t* ss = reinterpret_cast<const uint16_t*>(st + L.code_bytes);
-    const uint16_t* zz = reinterpret_cast<const uint16_t*>(st + L.code_bytes + L.sz_bytes);
-    float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [half][c]: m = r, weight row 8h + 2t + c
+    const uint2* my = slots + ((size_t)((j % kStages) * kCW + warp) * SL) * 32 + lane;
+    const uint2 sw = my[(2 * GPW) * 32], zw = my[(2 * GPW + 1) * 32];
+    const int b = j % kRed;
+    float y[4] = {0.f, 0.f, 0.f, 0.f};  // rows r, r, r+8, r+8; m = 2t, 2t+1, 2t, 2t+1
 #pragma unroll
-    for (int gi = 0; gi < kGpw; ++gi) {
-      if (gi >= ng) break;
-      const int g = g_begin + gi;
-      const int chunk = ((2 * (g & 3) + (t >> 1)) ^ r) << 4;
-      const uint8_t* box = st + (g >> 2) * 2048 + chunk + (t & 1) * 8;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint2 cw = *reinterpret_cast<const uint2*>(box + (8 * h + r) * 128);
+    for (int gi = 0; gi < GPW; ++gi) {
+      // the scale and zero words of group gi of rows r, r + 8 sit in lane
+      // 4 r + gi; the fp16 value is the half given by the element's parity
+      // (the same for rows r and r + 8: 8 G is even)
+      const int src = 4 * r + gi;
+      const int sh = (int)((((size_t)min(n0 + r, N - 1) * G + g_begin + gi) & 1) * 16);
+      const auto half_of = [&](uint32_t w) {
+        return __half2float(__ushort_as_half((unsigned short)((w >> sh) & 0xFFFFu)));
+      };
+      const float s_lo = half_of(__shfl_sync(0xFFFFFFFFu, sw.x, src));
+      const float s_hi = half_of(__shfl_sync(0xFFFFFFFFu, sw.y, src));
+      const float z_lo = half_of(__shfl_sync(0xFFFFFFFFu, zw.x, src)) + 128.0f;
+      const float z_hi = half_of(__shfl_sync(0xFFFFFFFFu, zw.y, src)) + 128.0f;
+      if (gi < ng) {
+        const uint2 cw0 = my[(2 * gi) * 32], cw1 = my[(2 * gi + 1) * 32];
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int p0 = 2 * jj, p1 = 2 * jj + 1;
-          const uint32_t b0 = nib2_to_bf16x2((p0 >> 2) ? cw.y : cw.x, 4 * (p0 & 3));
-          const uint32_t b1 = nib2_to_bf16x2((p1 >> 2) ? cw.y : cw.x, 4 * (p1 & 3));
-          mma_bf16_16816(d, afr[gi][p0], 0u, afr[gi][p1], 0u, b0, b1);
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t c0 = (v >> 1) ? cw0.y : cw0.x;
+          const uint32_t c1 = (v >> 1) ? cw1.y : cw1.x;
+          const int s0 = 8 * (v & 1);
+          mma_bf16_16816(d, nib2_biased(c0, s0), nib2_biased(c1, s0), nib2_biased(c0, s0 + 4),
+                         nib2_biased(c1, s0 + 4), bfr[gi][2 * v], bfr[gi][2 * v + 1]);
         }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int row = 8 * h + 2 * t + c;
-          const float s = __half2float(__ushort_as_half(ss[row * G + g]));
-          const float z = __half2float(__ushort_as_half(zz[row * G + g]));
-          y[h][c] = __fmaf_rn(s, __fmaf_rn(-z, sxr[gi], d[c]), y[h][c]);
-        }
+        y[0] = __fmaf_rn(s_lo, __fmaf_rn(-z_lo, sx[gi][0], d[0]), y[0]);
+        y[1] = __fmaf_rn(s_lo, __fmaf_rn(-z_lo, sx[gi][1], d[1]), y[1]);
+        y[2] = __fmaf_rn(s_hi, __fmaf_rn(-z_hi, sx[gi][0], d[2]), y[2]);
+        y[3] = __fmaf_rn(s_hi, __fmaf_rn(-z_hi, sx[gi][1], d[3]), y[3]);
       }
     }
-    float* rb = red + (size_t)(j & 1) * kWarps * 128;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) rb[(warp * 16 + 8 * h + 2 * t + c) * 8 + r] = y[h][c];
-    __syncthreads();  // stage `slot` fully read; partials complete
-    if (threadIdx.x == 0 && issued < my_tiles) {
-      fence_proxy_async_smem();
-      issue(issued);
-      ++issued;
+    // partials of tile j into buffer b once the reduction warp has read it
+    bool ok = mbar_wait(&red_empty[b], ((uint32_t)(j / kRed) & 1u) ^ 1u, dev_status, wait_ns) &&
+              !abort_flag;
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+      abort_flag = 1;
+      break;
     }
-    if (threadIdx.x < 128) {
-      const int row = threadIdx.x >> 3, m = threadIdx.x & 7;
-      if (m < M && n0 + row < N) {
-        float s = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += rb[(w * 16 + row) * 8 + m];
-        if (bias) s += __uint_as_float((uint32_t)bias[n0 + row] << 16);
-        Y[(size_t)m * N + n0 + row] = f32_to_bf16_rn(s);
-      }
-    }
+    if (lane == 0 && warp == 0) SVDQ_ATR(96, j);
+    *reinterpret_cast<float2*>(&red[b][warp][r * 8 + 2 * t]) = make_float2(y[0], y[1]);
+    *reinterpret_cast<float2*>(&red[b][warp][(r + 8) * 8 + 2 * t]) = make_float2(y[2], y[3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&red_full[b]);
+    if (lane == 0 && warp == 0) SVDQ_ATR(160, j);
   }
-  if (threadIdx.x == 0 && *abort_flag) {  // let issued copies land before exiting
-    for (int j = max(0, issued - stages); j < issued; ++j)
-      mbar_wait(&full[j % stages], (uint32_t)(j / stages) & 1u, nullptr, wait_ns);
-  }
+  cp_async_wait<0>();  // nothing may land in shared memory after the CTA exits
 }
 
 }  // namespace
 
-int awq_max_k() { return kWarps * kGpw * 64; }
+int awq_max_k() { return 4096; }  // 6 groups per compute warp at most
 
-cudaError_t launch_awq_gemv(const CUtensorMap& tm_q, const uint16_t* X, const uint16_t* scales,
+cudaError_t launch_awq_gemv(const uint8_t* qweight, const uint16_t* X, const uint16_t* scales,
                             const uint16_t* zeros, const uint16_t* bias, uint16_t* Y, int M,
                             int N, int K, int* dev_status, cudaStream_t stream, int num_sms) {
-  const AwqLayout L = awq_layout(K);
-  if (L.stages < 2 || K > awq_max_k()) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_awq_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+  if (K > awq_max_k() || K % 64 != 0) return cudaErrorInvalidValue;
+  const int gpw = (K / 64 + kCW - 1) / kCW;
+  auto kern = gpw <= 1 ? k_awq_gemv<1> : gpw == 2 ? k_awq_gemv<2> : gpw == 3 ? k_awq_gemv<3>
+             : gpw == 4 ? k_awq_gemv<4> : gpw == 5 ? k_awq_gemv<5> : k_awq_gemv<6>;
+  const int smem = gpw <= 1 ? awq_smem_bytes<1>() : gpw == 2 ? awq_smem_bytes<2>()
+                 : gpw == 3 ? awq_smem_bytes<3>() : gpw == 4 ? awq_smem_bytes<4>()
+                 : gpw == 5 ? awq_smem_bytes<5>() : awq_smem_bytes<6>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (N + 15) / 16;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  k_awq_gemv<<<grid, kThreads, L.smem, stream>>>(tm_q, X, scales, zeros, bias, Y, M, N, K,
-                                                 dev_status, kWaitTimeoutNs);
+  kern<<<grid, kThreads, smem, stream>>>(qweight, X, scales, zeros, bias, Y, M, N, K, dev_status,
+                                         kWaitTimeoutNs);
   return cudaGetLastError();
 }
 
 }  // namespace svdq
+
+#ifdef SVDQ_AWQ_TRACE
+// instrumented builds only: where the first 8 CTAs write their timeline
+// (512 x u64 per CTA), or nullptr to stop
+extern "C" int svdq_awq_trace_set(unsigned long long* p) {
+  return (int)cudaMemcpyToSymbol(svdq::g_awq_trace, &p, sizeof(p));
+}
+#endif

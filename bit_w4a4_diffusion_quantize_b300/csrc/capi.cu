@@ -213,7 +213,7 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
                            const uint16_t* scales, const uint16_t* zeros, const uint16_t* bias,
                            uint16_t* Y, int M, int N, int K, int group_size, int* dev_status,
                            void* stream) {
-  if (M < 1 || M > 8 || N < 8 || N % 8 != 0 || K <= 0 || K % 128 != 0 ||
+  if (M < 1 || M > 8 || N < 8 || N % 8 != 0 || K <= 0 || K % 64 != 0 ||
       K > svdq::awq_max_k() || group_size != 64)
     return SVDQ_ERR_SHAPE;
   if (!X_bf16 || !qweight || !scales || !zeros || !Y) return SVDQ_ERR_NULL;
@@ -223,11 +223,7 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
   int sms = 0;
   svdq_status st = current_device(nullptr, &sms);
   if (st != SVDQ_OK) return st;
-  CUtensorMap tm_q;
-  if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, qweight, (uint64_t)K / 2, (uint64_t)N,
-                 (uint64_t)K / 2, 128u, 16u, CU_TENSOR_MAP_SWIZZLE_128B))
-    return SVDQ_ERR_CUDA;
-  cudaError_t e = svdq::launch_awq_gemv(tm_q, X_bf16, scales, zeros, bias, Y, M, N, K,
+  cudaError_t e = svdq::launch_awq_gemv(qweight, X_bf16, scales, zeros, bias, Y, M, N, K,
                                         dev_status, static_cast<cudaStream_t>(stream), sms);
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }

@@ -183,6 +183,15 @@ SVDQ_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, in
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// 3-D tiled bulk tensor load global -> shared, completion on an mbarrier.
+SVDQ_DEVINL void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y,
+                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 SVDQ_DEVINL void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -221,6 +230,24 @@ SVDQ_DEVINL void cluster_sync() {
       "barrier.cluster.arrive.release.aligned;\n"
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
+}
+// hint: bring the 128-byte line at p into L2 (no data returned)
+SVDQ_DEVINL void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// per-thread asynchronous copy global -> shared of 4 or 8 bytes; src_bytes = 0
+// writes zeros (nothing is read)
+template <int BYTES>
+SVDQ_DEVINL void cp_async(void* smem_dst, const void* gsrc, int src_bytes) {
+  static_assert(BYTES == 4 || BYTES == 8, "cp.async.ca size");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc), "n"(BYTES), "r"(src_bytes)
+               : "memory");
+}
+SVDQ_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+SVDQ_DEVINL void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // 2-D tiled TMA store of a shared-memory box to global memory (bulk group)
 SVDQ_DEVINL void tma_store_2d(const void* tmap, const void* smem_src, int x, int y) {

@@ -30,8 +30,8 @@ cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a
 // Largest K the AWQ GEMV stages in shared memory.
 int awq_max_k();
 
-// qweight [N][K/2] bytes: box 128 x 16 rows, 128B swizzle.
-cudaError_t launch_awq_gemv(const CUtensorMap& tm_q, const uint16_t* X, const uint16_t* scales,
+// qweight [N][K/2] bytes (16-byte aligned).
+cudaError_t launch_awq_gemv(const uint8_t* qweight, const uint16_t* X, const uint16_t* scales,
                             const uint16_t* zeros, const uint16_t* bias, uint16_t* Y, int M,
                             int N, int K, int* dev_status, cudaStream_t stream, int num_sms);
 

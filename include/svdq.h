@@ -215,8 +215,8 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
  * fp32 accumulation.  Streams the 4-bit weights once from HBM.
  * Inputs: X [M][K] bf16; qweight [N][K/2] (even k in the low nibble);
  * scales, zeros [N][K/64] fp16; bias [N] bf16 (nullable).  Output Y [M][N] bf16.
- * Sizes: 1 <= M <= 8, N % 8 == 0 (N >= 8), K % 128 == 0, K <= 4096 (X and
- * its per-group sums are staged in shared memory), group_size == 64.
+ * Sizes: 1 <= M <= 8, N % 8 == 0 (N >= 8), K % 64 == 0, K <= 4096 (X and its
+ * per-group sums stay in registers), group_size == 64.
  * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_ALIGN,
  * SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA. */
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

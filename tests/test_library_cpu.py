@@ -96,8 +96,9 @@ def test_gemm_argument_errors():
 
 
 def test_awq_argument_errors():
-    assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(K=192) == -2 and _awq(g=128) == -2
+    assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(g=128) == -2
     assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
+    assert _awq(K=96) == -2  # K % 64 != 0
     assert _awq(X=P(0)) == -1 and _awq(X=MISALIGNED) == -3
 
 
