@@ -41,6 +41,41 @@ L2_BYTES = 126 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the attn_out workload, each valid only while the kernel's
+# sources hash to what was captured (the summaries are under profiles/).
+MEASURED_TRAFFIC = {
+    "svdq_gemm_w4a4": {
+        "bytes": 12889856 + 10496,
+        "sources": {"gemm_w4a4.cu": "d14d03692ec040d0ea8d435e6ff4d065ad9fb9f40213008ac91c20cf33544b9f",
+                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
+    "svdq_quantize_act": {
+        "bytes": 25392128 + 0,
+        "sources": {"quantize_act.cu": "29cdf2d442131197cb9f5c3ca44b7b3597b01bacd56ba2206a95368076e9b93c",
+                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
+    "awq_gemv_w4a16": {
+        "bytes": 31927296 + 0,
+        "sources": {"awq_gemv.cu": "afbda228fe8edcb611e5ac8ce0cfffed94e7d71bfd8d3aec56e1be18a5720435",
+                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "profile": "profiles/awq_gemv_w4a16_modulation_ncu.md"},
+}
+
+
+def measured_traffic(kernel: str):
+    """Bytes per launch from the recorded capture, or None if the kernel's
+    sources changed since."""
+    import hashlib
+    rec = MEASURED_TRAFFIC[kernel]
+    csrc = os.path.join(ROOT, "bit_w4a4_diffusion_quantize_b300", "csrc")
+    for name, digest in rec["sources"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return rec["bytes"]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,8 +295,8 @@ def run_gpu(args, world, rank, local):
         barrier(world)
         t_q = timed(g_q) / args.steps
         t_g = timed(g_g) / args.steps
-        # keep the same load running so the clock record spans >= 1 s of it
-        t_end = time.perf_counter() + max(0.0, 1.0 - (time.perf_counter() - wall0))
+        # keep the same load running so the clock record spans >= clock_window s
+        t_end = time.perf_counter() + max(0.0, args.clock_window - (time.perf_counter() - wall0))
         while time.perf_counter() < t_end:
             g_step.replay()
             torch.cuda.synchronize()
@@ -303,6 +338,19 @@ def run_gpu(args, world, rank, local):
     if args.awq_blocks > 0:
         awq = run_awq(args, lib, dev, stream, world)
 
+    # the tensor cores' own NVFP4 rate on this device: back-to-back
+    # M128 N256 K64 block-scaled MMAs on every SM (no memory traffic)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    iters = 8192
+    for _ in range(2):
+        lib.bench_mma_rate(0, 256, iters, sms, dev_status=status, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    lib.bench_mma_rate(0, 256, iters, sms, dev_status=status, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mma_tflops = 2.0 * 128 * 256 * 64 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
     pk = peaks()
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     g_avg = t_g
@@ -335,16 +383,21 @@ def run_gpu(args, world, rank, local):
             "frac": round(gemm_tflops / fp4_peak, 4),
             "peak_source": f"{pk['source']} bf16 {pk['bf16_tflops']} TFLOP/s x {FP4_OVER_BF16:g} "
                            "(nominal fp4/bf16 dense ratio)",
-            "traffic": None,
+            "traffic": measured_traffic("svdq_gemm_w4a4"),
+            "traffic_note": "ncu dram read+write of one launch (Y is written back from L2 "
+                            "after the kernel, so it is not in the count)",
             "algorithmic_bytes": g_bytes,
             "achieved_hbm_gbs": round(g_bytes / g_avg / 1e9, 1),
+            "measured_mma_tflops": round(mma_tflops, 1),
+            "frac_of_measured_mma": round(gemm_tflops / mma_tflops, 4),
         },
         "kernels": {
             "svdq_quantize_act": {"us": round(q_avg * 1e6, 2), "bound": "hbm",
                                   "achieved_gbs": round(q_bytes / q_avg / 1e9, 1),
                                   "peak_gbs": pk["hbm_gbs"],
                                   "frac": round(q_bytes / q_avg / 1e9 / pk["hbm_gbs"], 4),
-                                  "algorithmic_bytes": q_bytes},
+                                  "algorithmic_bytes": q_bytes,
+                                  "traffic": measured_traffic("svdq_quantize_act")},
             "svdq_gemm_w4a4": {"us": round(g_avg * 1e6, 2), "tflops": round(gemm_tflops, 1)},
         },
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in e2e.items()},
@@ -406,7 +459,10 @@ def run_awq(args, lib, dev, stream, world):
         res["launches"] += reps * len(blocks)
     res["roofline"] = {"bound": "hbm", "kernel": "awq_gemv_w4a16",
                        "achieved": res["by_M"]["1"]["gbs"] / world, "peak": pk["hbm_gbs"],
-                       "unit": "GB/s", "frac": res["by_M"]["1"]["frac"], "traffic": None}
+                       "unit": "GB/s", "frac": res["by_M"]["1"]["frac"],
+                       "traffic": measured_traffic("awq_gemv_w4a16"),
+                       "algorithmic_bytes_per_launch":
+                           N * K // 2 + 4 * N * (K // 64) + K * 2 + N * 2 + N * 2}
     return res
 
 
@@ -442,6 +498,8 @@ def main(argv=None):
     ap.add_argument("--awq-blocks", type=int, default=workloads.AWQ_BLOCKS)
     ap.add_argument("--oracle-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of repeated steps (untimed) over which clocks are sampled")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
