@@ -13,8 +13,8 @@
 // nibble OR-ed into the mantissa of 128.0, 0x4300: one shift and one logic op
 // per pair of codes); the constant 128 is folded into the zero point.  The
 // activations (M <= 8 rows) are the B operand (N = 8 of the MMA, nothing
-// wasted) and stay in registers for the whole kernel: each of the 12 compute
-// warps of a CTA owns a fixed range of K groups.  Per 64-group the fp32 sums
+// wasted) and stay in registers for the whole kernel: each compute warp of a
+// CTA owns a fixed range of at most 4 K groups.  Per 64-group the fp32 sums
 // get scale and zero point; sum_{k in g} x[m][k] is formed once per warp.
 //
 // Streaming.  The weights are read exactly once, by the compute warps
@@ -27,7 +27,7 @@
 // waiting for its own copies.  Scale and zero values reach the lanes that need
 // them through quad shuffles.  A persistent CTA walks tiles
 // blockIdx.x + j * gridDim.x.  The warps leave their fp32 partials in a ring
-// of reduction buffers (no CTA-wide barrier); a reduction warp adds the 12
+// of reduction buffers (no CTA-wide barrier); a reduction warp adds the
 // partials and the bias in a fixed order and writes Y.
 //
 // The k order inside an MMA is permuted: a lane feeds 16 consecutive k of a
@@ -45,8 +45,9 @@ namespace svdq {
 
 namespace {
 
-constexpr int kCW = 12;                   // compute warps
-constexpr int kThreads = 32 * (kCW + 1);  // + the reduction warp
+// compute warps per CTA: CW (12, or 16 when K > 3072), each owning at most
+// 4 K groups (one lane of a quad loads the scale words of one group); plus
+// one reduction warp
 constexpr int kRed = 4;  // reduction buffers (tiles whose partials may be in flight)
 constexpr int kStages = 4;  // tiles in flight per lane (cp.async groups)
 
@@ -75,9 +76,9 @@ struct Slots {
   static constexpr int kPerLane = 2 * GPW + 2;
   static constexpr int kWarpStage = kPerLane * 32;  // uint2 per warp and stage
 };
-template <int GPW>
+template <int GPW, int CW>
 constexpr int awq_smem_bytes() {
-  return kStages * kCW * Slots<GPW>::kWarpStage * 8;
+  return kStages * CW * Slots<GPW>::kWarpStage * 8;
 }
 
 #ifdef SVDQ_AWQ_TRACE
@@ -95,16 +96,17 @@ __device__ unsigned long long* g_awq_trace = nullptr;
   } while (0)
 #endif
 
-// GPW: K groups per compute warp at most (ceil(G / kCW), 1..6)
-template <int GPW>
-__global__ void __launch_bounds__(kThreads, 1)
+// GPW: K groups per compute warp at most (ceil(G / CW), 1..4)
+template <int GPW, int CW>
+__global__ void __launch_bounds__(32 * (CW + 1), 1)
     k_awq_gemv(const uint8_t* __restrict__ qw, const uint16_t* __restrict__ X,
                const uint16_t* __restrict__ sc, const uint16_t* __restrict__ zr,
                const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
                int* dev_status, uint64_t wait_ns) {
+  static_assert(GPW >= 1 && GPW <= 4, "a quad loads the scale words of at most 4 groups");
   extern __shared__ uint2 slots[];  // [stage][warp][slot][lane]
-  __shared__ __align__(16) float red[kRed][kCW][16 * 8];  // [buffer][warp][row * 8 + m]
-  __shared__ __align__(8) uint64_t red_full[kRed];        // count kCW
+  __shared__ __align__(16) float red[kRed][CW][16 * 8];  // [buffer][warp][row * 8 + m]
+  __shared__ __align__(8) uint64_t red_full[kRed];        // count CW
   __shared__ __align__(8) uint64_t red_empty[kRed];       // count 1
   __shared__ volatile uint32_t abort_flag;
   const int G = K / 64;
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < kRed; ++b) {
-      mbar_init(&red_full[b], kCW);
+      mbar_init(&red_full[b], CW);
       mbar_init(&red_empty[b], 1);
     }
     abort_flag = 0;
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  if (warp == kCW) {
+  if (warp == CW) {
     // ---------------------------------------------------------- reduction warp
     for (int j = 0; j < my_tiles; ++j) {
       const int b = j % kRed;
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m < M && n0 + row < N) {
           float s = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kCW; ++w) s += red[b][w][idx];
+          for (int w = 0; w < CW; ++w) s += red[b][w][idx];
           s += __uint_as_float(bv[i] << 16);
           Y[(size_t)m * N + n0 + row] = f32_to_bf16_rn(s);
         }
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // activation fragments of this warp's groups [g_begin, g_begin + ng): lane
   // (r, t) holds x[m = r][64 g + 16 t .. + 15] as the B operand of the 4 MMAs
   // of a group: MMA v takes k pairs (e, e + 4) and (e + 1, e + 5), e = 8 (v/2) + 2 (v%2)
-  const int g_begin = (warp * G) / kCW, ng = ((warp + 1) * G) / kCW - g_begin;
+  const int g_begin = (warp * G) / CW, ng = ((warp + 1) * G) / CW - g_begin;
   uint32_t bfr[GPW][8];
   float sx[GPW][2];  // sum over the group's 64 k of x[m] for m = 2t, 2t + 1
 #pragma unroll
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto issue = [&](int j) {
     if (j < my_tiles) {
       const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-      uint2* my = slots + ((size_t)((j % kStages) * kCW + warp) * SL) * 32 + lane;
+      uint2* my = slots + ((size_t)((j % kStages) * CW + warp) * SL) * 32 + lane;
       const int lo_b = n0 + r < N ? 8 : 0, hi_b = n0 + r + 8 < N ? 8 : 0;
       const uint8_t* q_lo = qw + (size_t)min(n0 + r, N - 1) * row_bytes + 8 * t;
       const uint8_t* q_hi = qw + (size_t)min(n0 + r + 8, N - 1) * row_bytes + 8 * t;
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     issue(j + kStages - 1);
     cp_async_wait<kStages - 1>();  // this lane's copies of tile j have landed
     const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-    const uint2* my = slots + ((size_t)((j % kStages) * kCW + warp) * SL) * 32 + lane;
+    const uint2* my = slots + ((size_t)((j % kStages) * CW + warp) * SL) * 32 + lane;
     const uint2 sw = my[(2 * GPW) * 32], zw = my[(2 * GPW + 1) * 32];
     const int b = j % kRed;
     float y[4] = {0.f, 0.f, 0.f, 0.f};  // rows r, r, r+8, r+8; m = 2t, 2t+1, 2t, 2t+1
@@ -287,24 +289,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int awq_max_k() { return 4096; }  // 6 groups per compute warp at most
+int awq_max_k() { return 4096; }  // 16 compute warps x 4 groups x 64
 
 cudaError_t launch_awq_gemv(const uint8_t* qweight, const uint16_t* X, const uint16_t* scales,
                             const uint16_t* zeros, const uint16_t* bias, uint16_t* Y, int M,
                             int N, int K, int* dev_status, cudaStream_t stream, int num_sms) {
   if (K > awq_max_k() || K % 64 != 0) return cudaErrorInvalidValue;
-  const int gpw = (K / 64 + kCW - 1) / kCW;
-  auto kern = gpw <= 1 ? k_awq_gemv<1> : gpw == 2 ? k_awq_gemv<2> : gpw == 3 ? k_awq_gemv<3>
-             : gpw == 4 ? k_awq_gemv<4> : gpw == 5 ? k_awq_gemv<5> : k_awq_gemv<6>;
-  const int smem = gpw <= 1 ? awq_smem_bytes<1>() : gpw == 2 ? awq_smem_bytes<2>()
-                 : gpw == 3 ? awq_smem_bytes<3>() : gpw == 4 ? awq_smem_bytes<4>()
-                 : gpw == 5 ? awq_smem_bytes<5>() : awq_smem_bytes<6>();
+  const int G = K / 64;
+  void (*kern)(const uint8_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+               const uint16_t*, uint16_t*, int, int, int, int*, uint64_t) = nullptr;
+  int smem = 0, threads = 0;
+#define SVDQ_AWQ_CASE(GPW_, CW_)                  \
+  {                                               \
+    kern = k_awq_gemv<GPW_, CW_>;                 \
+    smem = awq_smem_bytes<GPW_, CW_>();           \
+    threads = 32 * (CW_ + 1);                     \
+  }
+  if (G <= 12) SVDQ_AWQ_CASE(1, 12)
+  else if (G <= 24) SVDQ_AWQ_CASE(2, 12)
+  else if (G <= 36) SVDQ_AWQ_CASE(3, 12)
+  else if (G <= 48) SVDQ_AWQ_CASE(4, 12)  // K = 3072: one 128-byte line per warp and row
+  else SVDQ_AWQ_CASE(4, 16)
+#undef SVDQ_AWQ_CASE
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (N + 15) / 16;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, smem, stream>>>(qweight, X, scales, zeros, bias, Y, M, N, K, dev_status,
-                                         kWaitTimeoutNs);
+  kern<<<grid, threads, smem, stream>>>(qweight, X, scales, zeros, bias, Y, M, N, K, dev_status,
+                                        kWaitTimeoutNs);
   return cudaGetLastError();
 }
 

@@ -158,11 +158,13 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
     return SVDQ_ERR_ALIGN;
   svdq_status st = current_device(nullptr, nullptr);
   if (st != SVDQ_OK) return st;
-  CUtensorMap tm_x;
+  CUtensorMap tm_x, tm_l1s;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, X_bf16, (uint64_t)K, (uint64_t)M,
-                 (uint64_t)K * 2, 64u, 16u, CU_TENSOR_MAP_SWIZZLE_128B))
+                 (uint64_t)K * 2, 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_l1s, CU_TENSOR_MAP_DATA_TYPE_UINT16, L1s, (uint64_t)K, (uint64_t)rank,
+                 (uint64_t)K * 2, 64u, (uint32_t)rank, CU_TENSOR_MAP_SWIZZLE_128B))
     return SVDQ_ERR_CUDA;
-  cudaError_t e = svdq::launch_quantize_act(tm_x, L1s, inv_lambda, M, K, rank, a_codes,
+  cudaError_t e = svdq::launch_quantize_act(tm_x, tm_l1s, inv_lambda, M, K, rank, a_codes,
                                             a_scales, lora_act, dev_status,
                                             static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;

@@ -8,8 +8,9 @@
 
 namespace svdq {
 
-// tm_x: X [M][K] bf16, box 64 x 16 rows, 128B swizzle (built on the host per call)
-cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const uint16_t* L1s,
+// tm_x: X [M][K] bf16, box 64 x 32 rows, 128B swizzle; tm_l1s: L1s [rank][K]
+// bf16, box 64 x rank rows, 128B swizzle (both built on the host per call)
+cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s,
                                 const float* inv_lambda, int M, int K, int rank,
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                                 int* dev_status, cudaStream_t stream);

@@ -8,16 +8,17 @@
 //   scale byte     = RNE_e4m3( amax16(x_hat) / 6 )        exact quotient rounding
 //   code nibble    = RNE_e2m1( x_hat / s )                exact quotient rounding
 //
-// Work split.  A CTA owns 16 consecutive rows (one m16 tile) and all of K; its
-// 8 warps split K into contiguous ranges of 64-wide steps.  Each warp streams
-// its X range through a private TMA ring in shared memory: per step one
-// 16 x 64 bf16 tile of X (128-byte swizzle, so the fragment reads below are
-// free of bank conflicts) and the 64 matching floats of inv_lambda, landing on
-// one mbarrier.  In one step a thread (quad lane t, group g) holds 16
-// consecutive k of rows g and g+8: exactly one 16-element quantization block
-// per row.  The same registers are the A fragments of the m16n8k16 MMAs of the
-// down projection; the k order inside an MMA is permuted, and the B fragments
-// (L1s rows, k contiguous, read from L2 one step ahead) use the same
+// Work split.  A CTA owns 32 consecutive rows (two m16 tiles) and all of K;
+// its 8 warps split K into contiguous ranges of 64-wide steps.  Each warp
+// streams its range through a private TMA ring in shared memory: per step a
+// 32 x 64 bf16 tile of X, the rank x 64 slice of L1s (both with the 128-byte
+// swizzle, so the fragment reads below are free of bank conflicts) and the
+// 64 matching floats of inv_lambda, landing on one mbarrier.  In one step a
+// thread (quad lane t, group g) holds 16 consecutive k of rows g, g+8, g+16,
+// g+24: exactly one 16-element quantization block per row.  The same
+// registers are the A fragments of the m16n8k16 MMAs of the down projection
+// (two m tiles share each L1s fragment); the k order inside an MMA is
+// permuted, and the B fragments (L1s rows, k contiguous) use the same
 // permutation.  Partial lora sums of the 8 warps are added in a fixed order
 // through shared memory, then rounded once.
 //
@@ -45,21 +46,30 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
+constexpr int kRows = 32;  // rows per CTA (two m16 tiles)
+constexpr int kSmemBudget = 222 * 1024;
 
 template <int RANK>
 struct QCfg {
-  static constexpr int NT = RANK / 8;         // n8 tiles of the down projection
-  static constexpr int X_BYTES = 16 * 128;    // 16 rows x 64 bf16
+  static constexpr int NT = RANK / 8;            // n8 tiles of the down projection
+  static constexpr int X_BYTES = kRows * 128;    // 32 rows x 64 bf16
+  static constexpr int L_BYTES = RANK * 128;     // RANK rows x 64 bf16 of L1s
   static constexpr int INV_BYTES = 64 * 4;
-  static constexpr int TX_BYTES = X_BYTES + INV_BYTES;
+  static constexpr int TX_BYTES = X_BYTES + L_BYTES + INV_BYTES;
+  static constexpr int STAGE_ALL = kWarps * (X_BYTES + L_BYTES + INV_BYTES);
+  static constexpr int FIXED = 128 * 8 + kWarps * 4 * 8;  // reciprocal table, barriers
+  static constexpr int STAGES = (kSmemBudget - FIXED) / STAGE_ALL > 4
+                                    ? 4 : (kSmemBudget - FIXED) / STAGE_ALL;
   static constexpr int OFF_X = 0;                                   // [warps][stages] tiles
-  static constexpr int OFF_INV = kWarps * kStages * X_BYTES;        // [warps][stages] slices
-  static constexpr int OFF_TAB = OFF_INV + kWarps * kStages * INV_BYTES;  // [128] float2
+  static constexpr int OFF_L = OFF_X + kWarps * STAGES * X_BYTES;   // [warps][stages] slices
+  static constexpr int OFF_INV = OFF_L + kWarps * STAGES * L_BYTES;
+  static constexpr int OFF_TAB = OFF_INV + kWarps * STAGES * INV_BYTES;  // [128] float2
   static constexpr int OFF_BAR = OFF_TAB + 128 * 8;
-  static constexpr int OFF_RED = OFF_BAR + kWarps * kStages * 8;
-  static constexpr int RED_BYTES = kWarps * 16 * RANK * 4;
-  static constexpr int SMEM_BYTES = OFF_RED + RED_BYTES + 1024;     // + alignment slack
+  // the lora partials [warps][32 rows][RANK] fp32 reuse the X ring afterwards
+  static constexpr int RED_BYTES = kWarps * kRows * RANK * 4;
+  static_assert(RED_BYTES <= OFF_L, "reduction buffer fits the X ring");
+  static_assert(STAGES >= 2, "pipeline depth");
+  static constexpr int SMEM_BYTES = OFF_BAR + kWarps * 4 * 8 + 1024;  // + alignment slack
 };
 
 // RD(1/d) and RN((1 - RD(1/d) d) / d): the two-term reciprocal of d
@@ -108,61 +118,54 @@ SVDQ_DEVINL void load_row16(const uint8_t* tile, int row, int t, uint32_t (&w)[8
   w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
 }
 
-// L1s rows g + 8n, k0 .. k0+15 (16 bf16 each): B fragments of NT n-tiles
-template <int NT>
-SVDQ_DEVINL void load_l1s(const uint16_t* __restrict__ L1s, int K, int g, int k0,
-                          uint32_t (&b)[NT][8]) {
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const uint16_t* p = L1s + (size_t)(g + 8 * n) * K + k0;
-    const uint4 lo = ld_keep_v4(p), hi = ld_keep_v4(p + 8);
-    b[n][0] = lo.x; b[n][1] = lo.y; b[n][2] = lo.z; b[n][3] = lo.w;
-    b[n][4] = hi.x; b[n][5] = hi.y; b[n][6] = hi.z; b[n][7] = hi.w;
-  }
-}
-
 template <int RANK>
-__global__ void __launch_bounds__(kThreads, 2)
-    k_quantize_act(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ L1s,
-                   const float* __restrict__ inv_lambda, int M, int K,
-                   uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_scales,
+__global__ void __launch_bounds__(kThreads, 1)
+    k_quantize_act(const __grid_constant__ CUtensorMap tm_x,
+                   const __grid_constant__ CUtensorMap tm_l1s, const float* __restrict__ inv_lambda,
+                   int M, int K, uint8_t* __restrict__ a_codes, uint8_t* __restrict__ a_scales,
                    uint16_t* __restrict__ lora_act, int* dev_status, uint64_t wait_ns) {
   using C = QCfg<RANK>;
   constexpr int NT = C::NT;
+  constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int m0 = blockIdx.x * 16;
+  const int m0 = blockIdx.x * kRows;
   const int steps = K >> 6;
   const int s_begin = (warp * steps) / kWarps;
   const int nst = ((warp + 1) * steps) / kWarps - s_begin;
-  uint8_t* xring = smem + C::OFF_X + warp * kStages * C::X_BYTES;
-  uint8_t* iring = smem + C::OFF_INV + warp * kStages * C::INV_BYTES;
+  uint8_t* xring = smem + C::OFF_X + warp * S * C::X_BYTES;
+  uint8_t* lring = smem + C::OFF_L + warp * S * C::L_BYTES;
+  uint8_t* iring = smem + C::OFF_INV + warp * S * C::INV_BYTES;
   float2* tab = reinterpret_cast<float2*>(smem + C::OFF_TAB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * 4;
   const int C4 = K >> 6;  // 4-column scale groups per row
-  const int rowA = m0 + g, rowB = m0 + g + 8;
-  const bool okA = rowA < M, okB = rowB < M;
+  // rows of this thread: g, g + 8 (m tile 0), g + 16, g + 24 (m tile 1)
+  int row[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) row[q] = m0 + g + 8 * q;
 
   if (lane == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_l1s);
   }
   __syncwarp();
   int issued = 0;  // lane 0 only
   auto issue = [&](int i) {
-    const int slot = i % kStages;
+    const int slot = i % S;
     const int k0 = (s_begin + i) * 64;
     mbar_arrive_expect_tx(&bars[slot], (uint32_t)C::TX_BYTES);
     tma_load_2d(xring + slot * C::X_BYTES, &tm_x, &bars[slot], k0, m0);
+    tma_load_2d(lring + slot * C::L_BYTES, &tm_l1s, &bars[slot], k0, 0);
     bulk_load(iring + slot * C::INV_BYTES, inv_lambda + k0, (uint32_t)C::INV_BYTES, &bars[slot]);
   };
   if (lane == 0)
-    for (; issued < min(kStages, nst); ++issued) issue(issued);
+    for (; issued < min(S, nst); ++issued) issue(issued);
 
   // two-term reciprocals of the 127 positive e4m3 values (code 0: zeros)
   if (threadIdx.x < 128)
@@ -172,25 +175,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float2 r6 = recip2(6.0f);
   __syncthreads();
 
-  float acc[NT][4];
+  float acc[2][NT][4];
 #pragma unroll
-  for (int n = 0; n < NT; ++n)
+  for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[n][c] = 0.0f;
-  uint32_t bfr[NT][8];
-  if (nst > 0) load_l1s<NT>(L1s, K, g, s_begin * 64 + 16 * t, bfr);
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[mt][n][c] = 0.0f;
 
   int consumed = 0;
   for (int i = 0; i < nst; ++i) {
-    const int slot = i % kStages;
+    const int slot = i % S;
     const int step = s_begin + i;
     const int k0 = step * 64 + 16 * t;
-    const bool ok = mbar_wait(&bars[slot], (uint32_t)(i / kStages) & 1u, dev_status, wait_ns);
+    const bool ok = mbar_wait(&bars[slot], (uint32_t)(i / S) & 1u, dev_status, wait_ns);
     if (!__all_sync(0xFFFFFFFFu, ok)) break;  // warp-uniform abort on timeout
     const uint8_t* xt = xring + slot * C::X_BYTES;
-    uint32_t xa[8], xb[8];
-    load_row16(xt, g, t, xa);
-    load_row16(xt, g + 8, t, xb);
+    const uint8_t* lt = lring + slot * C::L_BYTES;
+    uint32_t xr[4][8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) load_row16(xt, g + 8 * q, t, xr[q]);
+    uint32_t bfr[NT][8];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) load_row16(lt, g + 8 * n, t, bfr[n]);
     float inv[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -204,69 +211,76 @@ __global__ void __launch_bounds__(kThreads, 2)
       issue(issued);
       ++issued;
     }
-    // ---- down projection: 4 k16 sub-steps x NT n-tiles
+    // ---- down projection: 2 m tiles x NT n tiles x 4 k16 sub-steps
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int j4 = 0; j4 < 4; ++j4)
-        mma_bf16_16816(acc[n], xa[2 * j4], xb[2 * j4], xa[2 * j4 + 1], xb[2 * j4 + 1],
-                       bfr[n][2 * j4], bfr[n][2 * j4 + 1]);
-    // the next step's L1s fragments: their L2 latency overlaps this step's
-    // quantization and the next tile's wait
-    if (i + 1 < nst) load_l1s<NT>(L1s, K, g, k0 + 64, bfr);
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j4 = 0; j4 < 4; ++j4)
+          mma_bf16_16816(acc[mt][n], xr[2 * mt][2 * j4], xr[2 * mt + 1][2 * j4],
+                         xr[2 * mt][2 * j4 + 1], xr[2 * mt + 1][2 * j4 + 1], bfr[n][2 * j4],
+                         bfr[n][2 * j4 + 1]);
     // ---- quantization: one block per row
-    uint2 ca, cb;
-    uint32_t sa, sb;
-    quant_block16(xa, inv, r6, tab, ca, sa);
-    quant_block16(xb, inv, r6, tab, cb, sb);
-    if (okA) *reinterpret_cast<uint2*>(a_codes + (size_t)rowA * (K >> 1) + (k0 >> 1)) = ca;
-    if (okB) *reinterpret_cast<uint2*>(a_codes + (size_t)rowB * (K >> 1) + (k0 >> 1)) = cb;
+    uint32_t sbyte[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint2 cq;
+      quant_block16(xr[q], inv, r6, tab, cq, sbyte[q]);
+      if (row[q] < M)
+        *reinterpret_cast<uint2*>(a_codes + (size_t)row[q] * (K >> 1) + (k0 >> 1)) = cq;
+    }
     // gather the 4 scale bytes of each row's 64-wide step across the quad;
-    // lane t = 0 writes row g's word, lane t = 1 row g+8's (tile layout:
-    // tile (r/128, c/4) of 512 bytes; entry (r%32)*16 + ((r/32)%4)*4 + c%4)
-    uint32_t wa = sa << (8 * t), wb = sb << (8 * t);
-    wa |= __shfl_xor_sync(0xFFFFFFFFu, wa, 1);
-    wa |= __shfl_xor_sync(0xFFFFFFFFu, wa, 2);
-    wb |= __shfl_xor_sync(0xFFFFFFFFu, wb, 1);
-    wb |= __shfl_xor_sync(0xFFFFFFFFu, wb, 2);
-    if (t < 2) {
-      const int r = t == 0 ? rowA : rowB;
-      if (r < M) {
-        const size_t off =
-            ((size_t)(r >> 7) * C4 + step) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-        *reinterpret_cast<uint32_t*>(a_scales + off) = t == 0 ? wa : wb;
-      }
+    // lane t writes row g + 8 t's word (tile layout: tile (r/128, c/4) of 512
+    // bytes; entry (r%32)*16 + ((r/32)%4)*4 + c%4)
+    uint32_t wq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      wq[q] = sbyte[q] << (8 * t);
+      wq[q] |= __shfl_xor_sync(0xFFFFFFFFu, wq[q], 1);
+      wq[q] |= __shfl_xor_sync(0xFFFFFFFFu, wq[q], 2);
+    }
+    const int r = row[t];
+    if (r < M) {
+      const uint32_t w = t == 0 ? wq[0] : t == 1 ? wq[1] : t == 2 ? wq[2] : wq[3];
+      const size_t off =
+          ((size_t)(r >> 7) * C4 + step) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+      *reinterpret_cast<uint32_t*>(a_scales + off) = w;
     }
   }
   if (lane == 0 && consumed < nst) {
     // timed out: let every copy already issued land before the CTA exits
     for (int i = consumed; i < issued; ++i)
-      mbar_wait(&bars[i % kStages], (uint32_t)(i / kStages) & 1u, nullptr, wait_ns);
+      mbar_wait(&bars[i % S], (uint32_t)(i / S) & 1u, nullptr, wait_ns);
   }
 
   // ---- reduce the warps' partial lora sums in a fixed order, round once
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int col = 8 * n + 2 * t;
-    float* base = red + ((size_t)warp * 16 + g) * RANK + col;
-    base[0] = acc[n][0];
-    base[1] = acc[n][1];
-    base[8 * RANK] = acc[n][2];
-    base[8 * RANK + 1] = acc[n][3];
-  }
+  // (the buffer reuses the X ring: every warp is done with it after the barrier)
   __syncthreads();
-  for (int idx = threadIdx.x; idx < 16 * RANK; idx += kThreads) {
+  float* red = reinterpret_cast<float*>(smem + C::OFF_X);
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int col = 8 * n + 2 * t;
+      float* base = red + ((size_t)warp * kRows + 16 * mt + g) * RANK + col;
+      base[0] = acc[mt][n][0];
+      base[1] = acc[mt][n][1];
+      base[8 * RANK] = acc[mt][n][2];
+      base[8 * RANK + 1] = acc[mt][n][3];
+    }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kRows * RANK; idx += kThreads) {
     float s = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += red[(size_t)w * 16 * RANK + idx];
-    const int r = m0 + idx / RANK;
-    if (r < M) lora_act[(size_t)m0 * RANK + idx] = f32_to_bf16_rn(s);
+    for (int w = 0; w < kWarps; ++w) s += red[(size_t)w * kRows * RANK + idx];
+    const int rr = m0 + idx / RANK;
+    if (rr < M) lora_act[(size_t)m0 * RANK + idx] = f32_to_bf16_rn(s);
   }
 }
 
 template <int RANK>
-cudaError_t launch_t(const CUtensorMap& tm_x, const uint16_t* L1s, const float* inv_lambda,
+cudaError_t launch_t(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s, const float* inv_lambda,
                      int M, int K, uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                      int* dev_status, cudaStream_t stream) {
   using C = QCfg<RANK>;
@@ -274,8 +288,8 @@ cudaError_t launch_t(const CUtensorMap& tm_x, const uint16_t* L1s, const float* 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int grid = (M + 15) / 16;
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_x, L1s, inv_lambda, M, K, a_codes,
+  const int grid = (M + kRows - 1) / kRows;
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tm_x, tm_l1s, inv_lambda, M, K, a_codes,
                                                    a_scales, lora_act, dev_status,
                                                    kWaitTimeoutNs);
   return cudaGetLastError();
@@ -283,20 +297,20 @@ cudaError_t launch_t(const CUtensorMap& tm_x, const uint16_t* L1s, const float* 
 
 }  // namespace
 
-cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const uint16_t* L1s,
+cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s,
                                 const float* inv_lambda, int M, int K, int rank,
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                                 int* dev_status, cudaStream_t stream) {
   switch (rank) {
     case 16:
-      return launch_t<16>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
-                          stream);
+      return launch_t<16>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
+                          dev_status, stream);
     case 32:
-      return launch_t<32>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
-                          stream);
+      return launch_t<32>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
+                          dev_status, stream);
     case 64:
-      return launch_t<64>(tm_x, L1s, inv_lambda, M, K, a_codes, a_scales, lora_act, dev_status,
-                          stream);
+      return launch_t<64>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
+                          dev_status, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -31,8 +31,11 @@ def test_awq_modulation_full_size(M):
     assert_y_close(_run(X, p, b), awq.awq_linear(X, p["qweight"], p["scales"], p["zeros"], b))
 
 
+# K covers every kernel variant: up to 1, 2, 3, 4 groups per compute warp with
+# 12 compute warps, and 16 compute warps above K = 3072
 @pytest.mark.parametrize("M,N,K", [(3, 200, 128), (1, 24, 64), (7, 1000, 640), (5, 4096, 192),
-                                   (8, 72, 1280), (6, 40, 960), (2, 1008, 4096)])
+                                   (8, 72, 1280), (6, 40, 960), (4, 136, 2048), (2, 1008, 4096),
+                                   (1, 56, 3584)])
 def test_awq_ragged(M, N, K):
     rng = np.random.default_rng(M * N + K)
     X = workloads.to_bf16_values(rng.standard_normal((M, K)).astype(np.float32))
