@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
     fence_mbar_init();
   }
   __syncthreads();
+  grid_dep_launch();
+  grid_dep_wait();  // the previous kernel's outputs (X among them) are complete
 
   if (warp == CW) {
     // ---------------------------------------------------------- reduction warp
@@ -314,9 +316,19 @@ cudaError_t launch_awq_gemv(const uint8_t* qweight, const uint16_t* X, const uin
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int tiles = (N + 15) / 16;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, threads, smem, stream>>>(qweight, X, scales, zeros, bias, Y, M, N, K, dev_status,
-                                        kWaitTimeoutNs);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, qweight, X, scales, zeros, bias, Y, M, N, K, dev_status,
+                         (uint64_t)kWaitTimeoutNs);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

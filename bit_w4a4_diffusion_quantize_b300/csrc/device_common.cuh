@@ -218,6 +218,15 @@ SVDQ_DEVINL void bulk_load_mc(void* smem_dst, const void* gsrc, uint32_t bytes, 
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream finishes.
+// grid_dep_wait blocks until that kernel has completed and its writes are
+// visible (a no-op otherwise): every global access of the library's kernels
+// comes after it, so only set-up work overlaps.  grid_dep_launch lets the
+// next kernel on the stream be scheduled early.
+SVDQ_DEVINL void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SVDQ_DEVINL void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 // ---------------------------------------------------------------- clusters
 SVDQ_DEVINL uint32_t cluster_ctarank() {
   uint32_t r;

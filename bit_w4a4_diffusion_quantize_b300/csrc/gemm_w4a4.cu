@@ -242,6 +242,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // the peer's barriers exist before anything is multicast to them
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  grid_dep_launch();
+  grid_dep_wait();  // the previous kernel's outputs (our inputs) are complete
 
   int issued = 0;  // producer lane only: ring slots filled
   if (warp == 0) {
@@ -493,17 +495,19 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
   // persistent: as many CTA pairs as can be resident at once (a GPC with an
   // odd number of free SMs leaves one idle), at most one per tile pair
   static int max_pairs = 0;
@@ -520,6 +524,7 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
   const int pairs_needed = ((m_tiles + 1) / 2) * (N / BN);
   const int pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, maps.a_codes, maps.w_codes, maps.lora, maps.l2s, a_scales,
                          w_scales, s_T, bias, Y, M, N, K, dev_status, test_stall,
                          (uint64_t)(test_stall ? 100000000ull : kWaitTimeoutNs));
