@@ -238,23 +238,25 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
     cp_async_wait<kStages - 1>();  // this lane's copies of tile j have landed
     const int n0 = (blockIdx.x + j * gridDim.x) * 16;
     const uint2* my = slots + ((size_t)((j % kStages) * CW + warp) * SL) * 32 + lane;
+    // this lane's scale and zero words (group t of rows r, r + 8) to fp32 once:
+    // the value is the half picked by its element index's parity (the same for
+    // rows r and r + 8: 8 G is even)
     const uint2 sw = my[(2 * GPW) * 32], zw = my[(2 * GPW + 1) * 32];
+    const int sh = ((min(n0 + r, N - 1) * G + g_begin + t) & 1) * 16;
+    const float s_lo_own = __half2float(__ushort_as_half((unsigned short)(sw.x >> sh)));
+    const float s_hi_own = __half2float(__ushort_as_half((unsigned short)(sw.y >> sh)));
+    const float z_lo_own = __half2float(__ushort_as_half((unsigned short)(zw.x >> sh))) + 128.0f;
+    const float z_hi_own = __half2float(__ushort_as_half((unsigned short)(zw.y >> sh))) + 128.0f;
     const int b = j % kRed;
     float y[4] = {0.f, 0.f, 0.f, 0.f};  // rows r, r, r+8, r+8; m = 2t, 2t+1, 2t, 2t+1
 #pragma unroll
     for (int gi = 0; gi < GPW; ++gi) {
-      // the scale and zero words of group gi of rows r, r + 8 sit in lane
-      // 4 r + gi; the fp16 value is the half given by the element's parity
-      // (the same for rows r and r + 8: 8 G is even)
+      // the scale and zero of group gi of rows r, r + 8 sit in lane 4 r + gi
       const int src = 4 * r + gi;
-      const int sh = (int)((((size_t)min(n0 + r, N - 1) * G + g_begin + gi) & 1) * 16);
-      const auto half_of = [&](uint32_t w) {
-        return __half2float(__ushort_as_half((unsigned short)((w >> sh) & 0xFFFFu)));
-      };
-      const float s_lo = half_of(__shfl_sync(0xFFFFFFFFu, sw.x, src));
-      const float s_hi = half_of(__shfl_sync(0xFFFFFFFFu, sw.y, src));
-      const float z_lo = half_of(__shfl_sync(0xFFFFFFFFu, zw.x, src)) + 128.0f;
-      const float z_hi = half_of(__shfl_sync(0xFFFFFFFFu, zw.y, src)) + 128.0f;
+      const float s_lo = __shfl_sync(0xFFFFFFFFu, s_lo_own, src);
+      const float s_hi = __shfl_sync(0xFFFFFFFFu, s_hi_own, src);
+      const float z_lo = __shfl_sync(0xFFFFFFFFu, z_lo_own, src);
+      const float z_hi = __shfl_sync(0xFFFFFFFFu, z_hi_own, src);
       if (gi < ng) {
         const uint2 cw0 = my[(2 * gi) * 32], cw1 = my[(2 * gi + 1) * 32];
         float d[4] = {0.f, 0.f, 0.f, 0.f};
