@@ -46,19 +46,19 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
 # sources hash to what was captured (the summaries are under profiles/).
 MEASURED_TRAFFIC = {
     "svdq_gemm_w4a4": {
-        "bytes": 12889856 + 10496,
-        "sources": {"gemm_w4a4.cu": "d14d03692ec040d0ea8d435e6ff4d065ad9fb9f40213008ac91c20cf33544b9f",
-                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "bytes": 12890368 + 5120,
+        "sources": {"gemm_w4a4.cu": "7c27d67a54caad6252a81852cd1425506068d7b621ebb7d639e80f08a9c89b01",
+                    "device_common.cuh": "848fde2c409e4fd5ffd83d5868f4d5a6722cab4666a9cf2290a4759a21741d4a"},
         "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
     "svdq_quantize_act": {
         "bytes": 25392128 + 0,
-        "sources": {"quantize_act.cu": "29cdf2d442131197cb9f5c3ca44b7b3597b01bacd56ba2206a95368076e9b93c",
-                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "sources": {"quantize_act.cu": "1ac727eb664eed2921ff4941ba6decbc109f896b8bda3fa0f110429d2869aac9",
+                    "device_common.cuh": "848fde2c409e4fd5ffd83d5868f4d5a6722cab4666a9cf2290a4759a21741d4a"},
         "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
-        "bytes": 31927296 + 0,
-        "sources": {"awq_gemv.cu": "afbda228fe8edcb611e5ac8ce0cfffed94e7d71bfd8d3aec56e1be18a5720435",
-                    "device_common.cuh": "bed930e376a373f6a25adcaf14678bd4d8982bc624526060a1df08e2085448d7"},
+        "bytes": 31926784 + 0,
+        "sources": {"awq_gemv.cu": "12ddbd740641a257e4f2cd7742cc83aca299283d64fc78ae470b033181542afa",
+                    "device_common.cuh": "848fde2c409e4fd5ffd83d5868f4d5a6722cab4666a9cf2290a4759a21741d4a"},
         "profile": "profiles/awq_gemv_w4a16_modulation_ncu.md"},
 }
 
