@@ -18,13 +18,14 @@
 // get scale and zero point; sum_{k in g} x[m][k] is formed once per warp.
 //
 // Streaming.  The weights are read exactly once, by the compute warps
-// themselves: for each 16-row tile a lane copies the code words it feeds to
-// its MMAs (8 bytes of rows r and r + 8 per group; 4 lanes cover 32
-// contiguous bytes of a row, every sector is used whole), and its scale and
-// zero words, with per-thread asynchronous copies (cp.async) into its own
-// shared-memory slots, kStages tiles ahead of its math: enough bytes in flight
-// for HBM rate, no registers held, and no synchronisation beyond each lane
-// waiting for its own copies.  Scale and zero values reach the lanes that need
+// themselves, kStages tiles ahead of their math with per-thread asynchronous
+// copies (cp.async): a warp copies its span of each of the tile's 16 code rows
+// (32 bytes per group) in 16-byte pieces, 8 consecutive lanes per 128-byte
+// line, into its own shared-memory area (rows of 128 bytes, pieces XOR-ed by
+// row % 8, so the fragment reads are conflict-free); each lane also copies
+// the scale and zero words of its group.  A lane waits for its own copies and
+// the warp synchronises: no CTA-wide barrier.  (Copying 8-byte pieces of 8
+// rows per instruction instead left the stream at a third of HBM rate.)  Scale and zero values reach the lanes that need
 // them through quad shuffles.  A persistent CTA walks tiles
 // blockIdx.x + j * gridDim.x.  The warps leave their fp32 partials in a ring
 // of reduction buffers (no CTA-wide barrier); a reduction warp adds the
@@ -67,18 +68,15 @@ SVDQ_DEVINL uint32_t ld_stream_u16(const uint16_t* p) {
   return v;
 }
 
-// shared-memory slots of one lane for one tile, 8 bytes each (lane-contiguous,
-// so every access is conflict-free): code words of rows r and r + 8 per group,
-// then the 4-byte words holding the scale and the zero of group t of rows r,
-// r + 8 (lanes t < groups; the fp16 value is the half picked by the index parity)
-template <int GPW>
-struct Slots {
-  static constexpr int kPerLane = 2 * GPW + 2;
-  static constexpr int kWarpStage = kPerLane * 32;  // uint2 per warp and stage
-};
+// shared memory of one warp for one tile: its 16 code rows (128 bytes each,
+// 16-byte pieces XOR-ed by row % 8), then per lane the 4-byte words holding the
+// scale of group t of rows r, r + 8 (8 bytes), then the same for the zeros
+// (lanes t < groups; the fp16 value is the half picked by the index parity)
+constexpr int kWarpCodeBytes = 16 * 128;
+constexpr int kWarpStageBytes = kWarpCodeBytes + 2 * 32 * 8;
 template <int GPW, int CW>
 constexpr int awq_smem_bytes() {
-  return kStages * CW * Slots<GPW>::kWarpStage * 8;
+  return kStages * CW * kWarpStageBytes;
 }
 
 #ifdef SVDQ_AWQ_TRACE
@@ -104,7 +102,7 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
                const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
                int* dev_status, uint64_t wait_ns) {
   static_assert(GPW >= 1 && GPW <= 4, "a quad loads the scale words of at most 4 groups");
-  extern __shared__ uint2 slots[];  // [stage][warp][slot][lane]
+  extern __shared__ __align__(128) uint8_t slots[];  // [stage][warp] kWarpStageBytes
   __shared__ __align__(16) float red[kRed][CW][16 * 8];  // [buffer][warp][row * 8 + m]
   __shared__ __align__(8) uint64_t red_full[kRed];        // count CW
   __shared__ __align__(8) uint64_t red_empty[kRed];       // count 1
@@ -130,16 +128,23 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
 
   if (warp == CW) {
     // ---------------------------------------------------------- reduction warp
-    for (int j = 0; j < my_tiles; ++j) {
-      const int b = j % kRed;
+    // the bias values of tile j are fetched three tiles ahead (a register
+    // ring), so that their memory latency stays off this warp's path
+    auto load_bias = [&](int j, uint32_t (&bv)[4]) {
       const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-      // the bias of tile j is fetched before its partials are waited for
-      uint32_t bv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (lane + 32 * i) >> 3;
-        bv[i] = (bias && n0 + row < N) ? ld_stream_u16(bias + n0 + row) : 0u;
+        bv[i] = (bias && j < my_tiles && n0 + row < N) ? ld_stream_u16(bias + n0 + row) : 0u;
       }
+    };
+    uint32_t bv[4], bv1[4], bv2[4];
+    load_bias(0, bv);
+    load_bias(1, bv1);
+    load_bias(2, bv2);
+    for (int j = 0; j < my_tiles; ++j) {
+      const int b = j % kRed;
+      const int n0 = (blockIdx.x + j * gridDim.x) * 16;
       const bool ok =
           mbar_wait(&red_full[b], (uint32_t)(j / kRed) & 1u, dev_status, wait_ns) && !abort_flag;
       if (!__all_sync(0xFFFFFFFFu, ok)) {
@@ -158,6 +163,12 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
           Y[(size_t)m * N + n0 + row] = f32_to_bf16_rn(s);
         }
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bv[i] = bv1[i];
+        bv1[i] = bv2[i];
+      }
+      load_bias(j + 3, bv2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[b]);
       if (lane == 0) SVDQ_ATR(64, j);
@@ -199,34 +210,42 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
   if (lane == 0 && warp == 0) SVDQ_ATR(2, 0);
 
   const size_t row_bytes = (size_t)K / 2;
-  constexpr int SL = Slots<GPW>::kPerLane;
+  // this lane's 16-byte code pieces of a tile: piece q = 32 i + lane is row
+  // q / (2 ng), chunk q % (2 ng) of the warp's span (16 rows x 2 ng chunks)
+  int pc_row[GPW], pc_src[GPW], pc_dst[GPW];
+#pragma unroll
+  for (int i = 0; i < GPW; ++i) {
+    const int q = 32 * i + lane;
+    const int row = q < 32 * ng ? q / (2 * ng) : -1, ch = q - (q / (2 * ng)) * 2 * ng;
+    pc_row[i] = row;
+    pc_src[i] = 32 * g_begin + 16 * ch;
+    pc_dst[i] = row * 128 + ((ch ^ (row & 7)) << 4);
+  }
   // asynchronous copies of tile j into stage j % kStages (one commit group per
   // tile, empty past the last tile, so that group counting stays uniform)
   auto issue = [&](int j) {
     if (j < my_tiles) {
       const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-      uint2* my = slots + ((size_t)((j % kStages) * CW + warp) * SL) * 32 + lane;
-      const int lo_b = n0 + r < N ? 8 : 0, hi_b = n0 + r + 8 < N ? 8 : 0;
-      const uint8_t* q_lo = qw + (size_t)min(n0 + r, N - 1) * row_bytes + 8 * t;
-      const uint8_t* q_hi = qw + (size_t)min(n0 + r + 8, N - 1) * row_bytes + 8 * t;
+      uint8_t* st = slots + (size_t)((j % kStages) * CW + warp) * kWarpStageBytes;
 #pragma unroll
-      for (int gi = 0; gi < GPW; ++gi) {
-        if (gi < ng) {
-          const size_t off = (size_t)(g_begin + gi) * 32;
-          cp_async<8>(my + (2 * gi) * 32, q_lo + off, lo_b);
-          cp_async<8>(my + (2 * gi + 1) * 32, q_hi + off, hi_b);
+      for (int i = 0; i < GPW; ++i) {
+        if (pc_row[i] >= 0) {
+          const int grow = n0 + pc_row[i];
+          cp_async16_cg(st + pc_dst[i], qw + (size_t)min(grow, N - 1) * row_bytes + pc_src[i],
+                        grow < N ? 16 : 0);
         }
       }
       if (t < ng) {
         // the 4-byte word holding element i (i & ~1, i | 1): inside the array,
         // whose element count N * G is even
+        const int lo_b = n0 + r < N ? 4 : 0, hi_b = n0 + r + 8 < N ? 4 : 0;
         const size_t i_lo = (size_t)min(n0 + r, N - 1) * G + g_begin + t;
         const size_t i_hi = (size_t)min(n0 + r + 8, N - 1) * G + g_begin + t;
-        uint32_t* w = reinterpret_cast<uint32_t*>(my + (2 * GPW) * 32);
-        cp_async<4>(w, sc + (i_lo & ~(size_t)1), lo_b ? 4 : 0);
-        cp_async<4>(w + 1, sc + (i_hi & ~(size_t)1), hi_b ? 4 : 0);
-        cp_async<4>(w + 64, zr + (i_lo & ~(size_t)1), lo_b ? 4 : 0);
-        cp_async<4>(w + 65, zr + (i_hi & ~(size_t)1), hi_b ? 4 : 0);
+        uint32_t* w = reinterpret_cast<uint32_t*>(st + kWarpCodeBytes) + 2 * lane;
+        cp_async<4>(w, sc + (i_lo & ~(size_t)1), lo_b);
+        cp_async<4>(w + 1, sc + (i_hi & ~(size_t)1), hi_b);
+        cp_async<4>(w + 64, zr + (i_lo & ~(size_t)1), lo_b);
+        cp_async<4>(w + 65, zr + (i_hi & ~(size_t)1), hi_b);
       }
     }
     cp_async_commit();
@@ -236,12 +255,14 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
   for (int j = 0; j < my_tiles; ++j) {
     issue(j + kStages - 1);
     cp_async_wait<kStages - 1>();  // this lane's copies of tile j have landed
+    __syncwarp();                  // ... and every lane's: the code rows are shared
     const int n0 = (blockIdx.x + j * gridDim.x) * 16;
-    const uint2* my = slots + ((size_t)((j % kStages) * CW + warp) * SL) * 32 + lane;
+    const uint8_t* st = slots + (size_t)((j % kStages) * CW + warp) * kWarpStageBytes;
     // this lane's scale and zero words (group t of rows r, r + 8) to fp32 once:
     // the value is the half picked by its element index's parity (the same for
     // rows r and r + 8: 8 G is even)
-    const uint2 sw = my[(2 * GPW) * 32], zw = my[(2 * GPW + 1) * 32];
+    const uint2 sw = *reinterpret_cast<const uint2*>(st + kWarpCodeBytes + 8 * lane);
+    const uint2 zw = *reinterpret_cast<const uint2*>(st + kWarpCodeBytes + 256 + 8 * lane);
     const int sh = ((min(n0 + r, N - 1) * G + g_begin + t) & 1) * 16;
     const float s_lo_own = __half2float(__ushort_as_half((unsigned short)(sw.x >> sh)));
     const float s_hi_own = __half2float(__ushort_as_half((unsigned short)(sw.y >> sh)));
@@ -258,7 +279,10 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
       const float z_lo = __shfl_sync(0xFFFFFFFFu, z_lo_own, src);
       const float z_hi = __shfl_sync(0xFFFFFFFFu, z_hi_own, src);
       if (gi < ng) {
-        const uint2 cw0 = my[(2 * gi) * 32], cw1 = my[(2 * gi + 1) * 32];
+        // bytes 32 gi + 8 t of the warp's span in rows r and r + 8
+        const uint8_t* cp = st + (((2 * gi + (t >> 1)) ^ r) << 4) + (t & 1) * 8;
+        const uint2 cw0 = *reinterpret_cast<const uint2*>(cp + r * 128);
+        const uint2 cw1 = *reinterpret_cast<const uint2*>(cp + (r + 8) * 128);
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int v = 0; v < 4; ++v) {

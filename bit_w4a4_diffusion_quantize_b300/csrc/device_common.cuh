@@ -272,6 +272,12 @@ SVDQ_DEVINL void cp_async(void* smem_dst, const void* gsrc, int src_bytes) {
                "l"(gsrc), "n"(BYTES), "r"(src_bytes)
                : "memory");
 }
+// 16 bytes, cached in L2 only (read-once streams)
+SVDQ_DEVINL void cp_async16_cg(void* smem_dst, const void* gsrc, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc), "r"(src_bytes)
+               : "memory");
+}
 SVDQ_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 SVDQ_DEVINL void cp_async_wait() {
