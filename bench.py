@@ -11,7 +11,9 @@ svdq_pack_weights (not timed).  Inputs rotate over enough buffer sets that
 every step reads from HBM, not L2.
 
 The AWQ phase times the 57 stacked adaLN modulation GEMVs (K = 3072,
-N = 6 x 3072, M in {1, 2, 4}) back to back.
+N = 6 x 3072, M in {1, 2, 4}) back to back; the MLP phase times the MLP's
+first linear (M = 4096, K = 3072, N = 12288) with GELU fused into its epilogue
+against the same GEMM without it.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
@@ -49,7 +51,8 @@ MEASURED_TRAFFIC = {
         "bytes": 12890368 + 7936,
         "sources": {"gemm_w4a4.cu": "7c27d67a54caad6252a81852cd1425506068d7b621ebb7d639e80f08a9c89b01",
                     "device_common.cuh": "14fcfcad0223e45a87c376a282b794f821e828b7c0b6681df40e12e424363a88"},
-        "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
+        "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md",
+        "note": "captured before the GELU epilogue variant was added to gemm_w4a4.cu"},
     "svdq_quantize_act": {
         "bytes": 25392128 + 0,
         "sources": {"quantize_act.cu": "1ac727eb664eed2921ff4941ba6decbc109f896b8bda3fa0f110429d2869aac9",
@@ -411,7 +414,73 @@ def run_gpu(args, world, rank, local):
     if awq is not None:
         line["awq"] = awq
         line["gpu_launches"] += awq["launches"]
+    if not args.no_mlp_gelu:
+        mlp = run_mlp_gelu(args, lib, dev, stream, world)
+        line["mlp_fc1_gelu"] = mlp
+        line["gpu_launches"] += mlp["launches"]
     return line
+
+
+def run_mlp_gelu(args, lib, dev, stream, world):
+    """The MLP's first linear (fc1: M = 4096, K = 3072, N = 12288, rank 32)
+    with GELU fused into the GEMM epilogue (svdq_gemm_w4a4_gelu), against the
+    plain GEMM on the same quantized operands.  A separate GELU pass would
+    read and write the M x N bf16 output once more."""
+    import torch
+    case = workloads.CASES["fc1"]
+    M, K, N, r = case.M, case.K, case.N, case.rank
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    Xbits = workloads.bf16_bits_of(X)
+    packed = lib.svdq_pack_weights(W, lib.svdq_calib_absmax(Xbits), r)
+
+    def dbits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sets = []
+    for _ in range(3):        # three weight + output sets (> 3 x L2 in all), rotated
+        s = {"wc": torch.from_numpy(packed["w_codes"]).to(dev),
+             "ws": torch.from_numpy(packed["w_scales"]).to(dev),
+             "L2s": dbits(packed["L2s"]), "bias": dbits(workloads.bf16_bits_of(b)),
+             "Y": torch.empty((M, N), dtype=torch.bfloat16, device=dev)}
+        s["ac"], s["as"], s["lora"] = lib.svdq_quantize_act(
+            dbits(Xbits).view(M, K), torch.from_numpy(packed["inv_lambda"]).to(dev),
+            dbits(packed["L1s"]), r, dev_status=status, stream=stream)
+        sets.append(s)
+
+    def launch(fn, i, st):
+        s = sets[i % len(sets)]
+        fn(s["ac"], s["as"], s["wc"], s["ws"], packed["w_tensor_scale"], s["lora"], s["L2s"],
+           s["bias"], M, N, K, r, s["Y"], dev_status=status, stream=st)
+
+    res = {"workload": f"fc1: SVDQ W4A4 linear + GELU (tanh) M={M} K={K} N={N} rank={r}",
+           "launches": 0}
+    for name, fn in (("gelu", lib.svdq_gemm_w4a4_gelu), ("plain", lib.svdq_gemm_w4a4)):
+        for i in range(args.warmup):
+            launch(fn, i, stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(dev)
+            for i in range(args.steps):
+                launch(fn, i, cs)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world, dev)
+        res[f"us_{name}"] = round(t * 1e6, 2)
+        res[f"tflops_{name}"] = round(world * 2.0 * M * N * K / t / 1e12, 1)
+        res["launches"] += args.steps
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the fc1 GELU phase")
+    res["gelu_epilogue_cost"] = round(res["us_gelu"] / res["us_plain"] - 1.0, 4)
+    res["separate_gelu_bytes_avoided"] = 2 * M * N * 2
+    return res
 
 
 def run_awq(args, lib, dev, stream, world):
@@ -498,6 +567,8 @@ def main(argv=None):
     ap.add_argument("--awq-blocks", type=int, default=workloads.AWQ_BLOCKS)
     ap.add_argument("--oracle-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mlp-gelu", action="store_true",
+                    help="skip the fc1 + fused GELU phase")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of repeated steps (untimed) over which clocks are sampled")
     args = ap.parse_args(argv)

@@ -46,6 +46,8 @@ _SIGS = {
                                  _c_p]),
     "svdq_gemm_w4a4": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _i32,
                               _i32, _i32, _i32, _c_p, _c_p]),
+    "svdq_gemm_w4a4_gelu": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p,
+                                   _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
@@ -185,22 +187,37 @@ def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None
     return a_codes, a_scales, lora_act
 
 
-def svdq_gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act, L2s,
-                   bias, M: int, N: int, K: int, rank: int, Y=None, dev_status=None,
-                   stream=None):
-    """L2s: [N, rank] bf16 = L2^T / s_T.  Returns Y [M, N] bf16 (CUDA)."""
+def _gemm(name, a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, M,
+          N, K, rank, Y, dev_status, stream):
     torch = _torch()
     for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
                  (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias")):
         _check_cuda(t, n)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
-    st = _lib.svdq_gemm_w4a4(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales),
+    st = getattr(_lib, name)(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales),
                              float(w_tensor_scale), _dptr(lora_act), _dptr(L2s), _dptr(bias),
                              _dptr(Y), int(M), int(N), int(K), int(rank), _dptr(dev_status),
                              _stream_ptr(stream))
-    _check(st, "svdq_gemm_w4a4")
+    _check(st, name)
     return Y
+
+
+def svdq_gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act, L2s,
+                   bias, M: int, N: int, K: int, rank: int, Y=None, dev_status=None,
+                   stream=None):
+    """L2s: [N, rank] bf16 = L2^T / s_T.  Returns Y [M, N] bf16 (CUDA)."""
+    return _gemm("svdq_gemm_w4a4", a_codes, a_scales, w_codes, w_scales, w_tensor_scale,
+                 lora_act, L2s, bias, M, N, K, rank, Y, dev_status, stream)
+
+
+def svdq_gemm_w4a4_gelu(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act,
+                        L2s, bias, M: int, N: int, K: int, rank: int, H=None, dev_status=None,
+                        stream=None):
+    """svdq_gemm_w4a4 followed by GELU (tanh form) in its epilogue: returns
+    H = bf16(gelu_tanh(Y)) [M, N] (CUDA)."""
+    return _gemm("svdq_gemm_w4a4_gelu", a_codes, a_scales, w_codes, w_scales, w_tensor_scale,
+                 lora_act, L2s, bias, M, N, K, rank, H, dev_status, stream)
 
 
 def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None,

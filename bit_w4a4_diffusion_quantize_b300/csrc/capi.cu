@@ -170,11 +170,14 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 
-svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
-                           const uint8_t* w_codes, const uint8_t* w_scales,
-                           float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2s,
-                           const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
-                           int* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+                      const uint8_t* w_scales, float w_tensor_scale, const uint16_t* lora_act,
+                      const uint16_t* L2s, const uint16_t* bias, uint16_t* Y, int M, int N,
+                      int K, int rank, bool gelu, int* dev_status, void* stream) {
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
   if (!rank_ok(rank)) return SVDQ_ERR_RANK;
   {
@@ -206,9 +209,31 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
   const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
   const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
-                                         bias, Y, M, N, K, rank, dev_status, test_stall, sms,
-                                         static_cast<cudaStream_t>(stream));
+                                         bias, Y, M, N, K, rank, gelu, dev_status, test_stall,
+                                         sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
+                           const uint8_t* w_codes, const uint8_t* w_scales,
+                           float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2s,
+                           const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
+                           int* dev_status, void* stream) {
+  return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, Y,
+                   M, N, K, rank, false, dev_status, stream);
+}
+
+svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
+                                const uint8_t* w_codes, const uint8_t* w_scales,
+                                float w_tensor_scale, const uint16_t* lora_act,
+                                const uint16_t* L2s, const uint16_t* bias, uint16_t* H, int M,
+                                int N, int K, int rank, int* dev_status, void* stream) {
+  return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, H,
+                   M, N, K, rank, true, dev_status, stream);
 }
 
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

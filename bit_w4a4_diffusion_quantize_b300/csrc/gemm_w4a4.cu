@@ -8,6 +8,10 @@
 //                                                     one fp32 TMEM accumulator
 //   Y    = bf16( s_T * acc + bias[n] )        with L2s = L2 / s_T (exact: s_T is
 //                                             a power of two)
+//   or H = bf16( gelu_tanh(Y) )               the GELU variant, for the first
+//                                             linear of a transformer MLP
+//                                             (dothoosh.com, same article: the
+//                                             full engine's GELU/MLP kernels)
 //
 // Persistent kernel in clusters of two CTAs (one CTA per SM).  A cluster walks
 // pairs of 128 x BN output tiles that share their columns (BN = 256, or 128
@@ -138,9 +142,37 @@ __device__ unsigned long long* g_gemm_trace = nullptr;
   } while (0)
 #endif
 
+SVDQ_DEVINL float ex2_approx(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+
+SVDQ_DEVINL float rcp_approx(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
+}
+
+// GELU in its tanh form, 0.5 y (1 + tanh(u)) with u = sqrt(2/pi) (y + 0.044715
+// y^3), for finite y.  0.5 (1 + tanh(u)) is the logistic function of 2u, so the
+// value is y / (1 + 2^t) with t = -2 u log2(e) = y (c1 + c2 y^2): no 1 + tanh
+// cancellation for negative y, no overflow (2^t = inf gives y * 0).  Relative
+// error about 2^-21 + |t| 2^-23 (ex2 and rcp approximations, 5 roundings),
+// far below a bf16 half-ulp where the value is not negligible.
+SVDQ_DEVINL float gelu_tanh_f32(float y) {
+  constexpr float c1 = -2.302208198144325f;   // -2 sqrt(2/pi) log2(e)
+  constexpr float c2 = -0.1029432395800235f;  // c1 * 0.044715
+  const float t = y * __fmaf_rn(c2, y * y, c1);
+  return y * rcp_approx(1.0f + ex2_approx(t));
+}
+
 // y = s_T * acc + bias for 32 accumulator columns (raw fp32 bits in v), as 16
 // bf16 pairs (round to nearest even); bias: 32 bf16 in shared memory or nullptr
-// (out may alias v: element i of out is written after v[2i], v[2i+1] are read)
+// (out may alias v: element i of out is written after v[2i], v[2i+1] are read).
+// GELU: the pairs hold bf16(gelu(y_b)) of the rounded y_b instead, the value
+// an unfused GELU would compute on the bf16 output of this layer.
+template <bool GELU>
 SVDQ_DEVINL void pack_cols32(const uint32_t* v, float s_T, const uint16_t* bias, uint32_t* out) {
 #pragma unroll
   for (int c8 = 0; c8 < 4; ++c8) {
@@ -152,7 +184,11 @@ SVDQ_DEVINL void pack_cols32(const uint32_t* v, float s_T, const uint16_t* bias,
       const int e = 8 * c8 + 2 * i;
       const float y0 = __fmaf_rn(s_T, __uint_as_float(v[e]), bf16lo_to_f32(bb[i]));
       const float y1 = __fmaf_rn(s_T, __uint_as_float(v[e + 1]), bf16hi_to_f32(bb[i]));
-      const __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);  // .x (low half) = y0
+      __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);  // .x (low half) = y0
+      if constexpr (GELU) {
+        const float2 yb = __bfloat1622float2(p);
+        p = __floats2bfloat162_rn(gelu_tanh_f32(yb.x), gelu_tanh_f32(yb.y));
+      }
       out[4 * c8 + i] = *reinterpret_cast<const uint32_t*>(&p);
     }
   }
@@ -181,7 +217,7 @@ SVDQ_DEVINL void transpose_chunks(uint32_t (&c)[4 * CH], int lane) {
   }
 }
 
-template <int BN, int RANK>
+template <int BN, int RANK, bool GELU>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_w4a4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_lora,
@@ -449,7 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // bf16 pairs in place: pair i lands in v[i] (read from v[2i], v[2i+1])
 #pragma unroll
       for (int c = 0; c < C::EPI_COLS / 32; ++c)
-        pack_cols32(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr, &v[16 * c]);
+        pack_cols32<GELU>(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr, &v[16 * c]);
       uint32_t(&pk)[4 * CH] = *reinterpret_cast<uint32_t(*)[4 * CH]>(&v[0]);
       if (bsm) {
         __syncwarp();
@@ -486,12 +522,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, int RANK>
+template <int BN, int RANK, bool GELU>
 cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
                      float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
                      int* dev_status, int test_stall, int num_sms, cudaStream_t stream) {
   using C = Cfg<BN, RANK>;
-  auto kern = k_gemm_w4a4<BN, RANK>;
+  auto kern = k_gemm_w4a4<BN, RANK, GELU>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -536,12 +572,14 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
 
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
-                             uint16_t* Y, int M, int N, int K, int rank, int* dev_status,
-                             int test_stall, int num_sms, cudaStream_t stream) {
+                             uint16_t* Y, int M, int N, int K, int rank, bool gelu,
+                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream) {
 #define SVDQ_GEMM_CASE(BN_, R_)                                                              \
   if (block_n == BN_ && rank == R_)                                                          \
-    return launch_t<BN_, R_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N, K,     \
-                             dev_status, test_stall, num_sms, stream);
+    return gelu ? launch_t<BN_, R_, true>(maps, a_scales, w_scales, w_tensor_scale, bias, Y,  \
+                                          M, N, K, dev_status, test_stall, num_sms, stream)  \
+                : launch_t<BN_, R_, false>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, \
+                                           M, N, K, dev_status, test_stall, num_sms, stream);
   SVDQ_GEMM_CASE(256, 16)
   SVDQ_GEMM_CASE(256, 32)
   SVDQ_GEMM_CASE(256, 64)

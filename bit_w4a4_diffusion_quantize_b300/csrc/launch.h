@@ -15,7 +15,7 @@ cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                                 int* dev_status, cudaStream_t stream);
 
-// Tensor maps of svdq_gemm_w4a4.
+// Tensor maps of svdq_gemm_w4a4 (and of its GELU variant).
 struct GemmMaps {
   CUtensorMap a_codes;  // [M][K/2] bytes: box 128 x 128 rows, 128B swizzle
   CUtensorMap w_codes;  // [N][K/2] bytes: box 128 x BN/2 rows (one CTA's half), 128B swizzle
@@ -25,8 +25,8 @@ struct GemmMaps {
 
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
-                             uint16_t* Y, int M, int N, int K, int rank, int* dev_status,
-                             int test_stall, int num_sms, cudaStream_t stream);
+                             uint16_t* Y, int M, int N, int K, int rank, bool gelu,
+                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream);
 
 // Largest K the AWQ GEMV stages in shared memory.
 int awq_max_k();

@@ -39,16 +39,19 @@ class SVDQLinear:
                    device="cuda"):
         return cls(_lib.svdq_pack_weights(W, x_absmax, rank), bias_bf16_bits, device)
 
-    def forward(self, X, out=None, act_buffers=None, dev_status=None, stream=None):
+    def forward(self, X, out=None, act_buffers=None, dev_status=None, stream=None,
+                gelu=False):
+        """gelu=True returns bf16(gelu_tanh(Y)) (svdq_gemm_w4a4_gelu): the
+        first linear of a transformer MLP with its activation fused."""
         M = X.shape[0]
         bufs = act_buffers or (None, None, None)
         a_codes, a_scales, lora = _lib.svdq_quantize_act(
             X, self.inv_lambda, self.L1s, self.rank, *bufs, dev_status=dev_status,
             stream=stream)
-        return _lib.svdq_gemm_w4a4(a_codes, a_scales, self.w_codes, self.w_scales,
-                                   self.w_tensor_scale, lora, self.L2s, self.bias, M, self.N,
-                                   self.K, self.rank, Y=out, dev_status=dev_status,
-                                   stream=stream)
+        gemm = _lib.svdq_gemm_w4a4_gelu if gelu else _lib.svdq_gemm_w4a4
+        return gemm(a_codes, a_scales, self.w_codes, self.w_scales, self.w_tensor_scale, lora,
+                    self.L2s, self.bias, M, self.N, self.K, self.rank, out,
+                    dev_status=dev_status, stream=stream)
 
     __call__ = forward
 

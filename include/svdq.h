@@ -209,6 +209,24 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
                            int M, int N, int K, int rank, int* dev_status,
                            void* stream);
 
+/* svdq_gemm_w4a4 with GELU (tanh form) fused into its epilogue, for the first
+ * linear of a transformer MLP (dothoosh.com, "How Nunchaku Lite halves the
+ * VRAM of diffusion models": the full engine's fused GELU/MLP kernels):
+ *   H = bf16( gelu_tanh( Y ) ),  gelu_tanh(y) = 0.5 y (1 + tanh( sqrt(2/pi)
+ *                                               (y + 0.044715 y^3) ))
+ * where Y is exactly the bf16 output svdq_gemm_w4a4 returns for the same
+ * arguments (GELU acts on the rounded value, as an unfused GELU on that output
+ * would); gelu_tanh is evaluated in fp32 (relative error below 2^-16 for
+ * |y| <= 8; the values beyond that are y itself or negligible), then rounded to
+ * nearest even.  H [M][N] bf16 takes the place of Y; every other argument,
+ * size rule and error is that of svdq_gemm_w4a4. */
+svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
+                                const uint8_t* w_codes, const uint8_t* w_scales,
+                                float w_tensor_scale, const uint16_t* lora_act,
+                                const uint16_t* L2s, const uint16_t* bias, uint16_t* H,
+                                int M, int N, int K, int rank, int* dev_status,
+                                void* stream);
+
 /* AWQ W4A16 GEMV for the small-M modulation layers (kernel-family list:
  * memory-bound adaLN modulation):
  *   Y[m][n] = bf16( sum_k X[m][k] (q[n][k] - z[n][k/64]) s[n][k/64] + bias[n] )

@@ -1,5 +1,6 @@
 """Host-side logic of bench.py, on CPU: the reference arm's JSON line, the
 recorded-traffic provenance check, and the clock-sample summary."""
+import hashlib
 import io
 import json
 import os
@@ -31,12 +32,21 @@ def test_reference_arm_prints_one_line_with_the_contract_keys():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
 
 
+def _sha(name):
+    with open(os.path.join(ROOT, "bit_w4a4_diffusion_quantize_b300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
 def test_recorded_traffic_is_void_once_a_source_changes(monkeypatch):
-    for kernel in bench.MEASURED_TRAFFIC:
-        assert isinstance(bench.measured_traffic(kernel), int)
+    for kernel, rec in bench.MEASURED_TRAFFIC.items():
+        current = all(_sha(n) == d for n, d in rec["sources"].items())
+        assert bench.measured_traffic(kernel) == (rec["bytes"] if current else None), kernel
+        assert os.path.exists(os.path.join(ROOT, rec["profile"])), rec["profile"]
     rec = dict(bench.MEASURED_TRAFFIC["svdq_gemm_w4a4"])
-    rec["sources"] = dict(rec["sources"], **{"gemm_w4a4.cu": "0" * 64})
+    rec["sources"] = {n: _sha(n) for n in rec["sources"]}
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, "svdq_gemm_w4a4", rec)
+    assert bench.measured_traffic("svdq_gemm_w4a4") == rec["bytes"]
+    rec["sources"] = dict(rec["sources"], **{"gemm_w4a4.cu": "0" * 64})
     assert bench.measured_traffic("svdq_gemm_w4a4") is None
 
 

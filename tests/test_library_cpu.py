@@ -5,6 +5,7 @@ validity where it is not: the SVD factors are unique only up to rotation and
 rounding, so the packed codes are checked to be exactly the quantization of
 the residual of the packer's own factors)."""
 import ctypes
+import functools
 import glob
 import os
 import re
@@ -34,7 +35,8 @@ def _declared_functions():
 
 def test_library_exports_every_declared_symbol():
     names = _declared_functions()
-    assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "awq_gemv_w4a16",
+    assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu",
+            "awq_gemv_w4a16",
             "awq_pack_weights", "svdq_calib_absmax", "svdq_check_device",
             "svdq_status_string"} <= names
     raw = ctypes.CDLL(lib.LIB_PATH)
@@ -67,9 +69,10 @@ def _qa(X=ALIGNED, inv=ALIGNED, l1=ALIGNED, M=64, K=256, r=32, codes=ALIGNED, sc
     return lib.raw_lib().svdq_quantize_act(X, inv, l1, M, K, r, codes, sc, lora, None, None)
 
 
-def _gemm(M=64, N=256, K=256, r=32, sT=2.0 ** -10, Y=ALIGNED, a=ALIGNED, bias=None):
-    return lib.raw_lib().svdq_gemm_w4a4(a, ALIGNED, ALIGNED, ALIGNED, ctypes.c_float(sT),
-                                        ALIGNED, ALIGNED, bias, Y, M, N, K, r, None, None)
+def _gemm(M=64, N=256, K=256, r=32, sT=2.0 ** -10, Y=ALIGNED, a=ALIGNED, bias=None,
+          fn="svdq_gemm_w4a4"):
+    return getattr(lib.raw_lib(), fn)(a, ALIGNED, ALIGNED, ALIGNED, ctypes.c_float(sT),
+                                      ALIGNED, ALIGNED, bias, Y, M, N, K, r, None, None)
 
 
 def _awq(M=1, N=64, K=256, g=64, X=ALIGNED):
@@ -85,14 +88,16 @@ def test_quantize_act_argument_errors():
     assert _qa(M=0, X=P(0)) == 0  # empty input: nothing to do
 
 
-def test_gemm_argument_errors():
-    assert _gemm(N=200) == -2 and _gemm(K=200) == -2 and _gemm(M=-3) == -2
-    assert _gemm(r=24) == -6
-    assert _gemm(sT=3.0) == -7 and _gemm(sT=float("inf")) == -7 and _gemm(sT=0.0) == -7
-    assert _gemm(sT=2.0 ** -101) == -7 and _gemm(sT=2.0 ** 101) == -7
-    assert _gemm(Y=P(0)) == -1
-    assert _gemm(a=MISALIGNED) == -3 and _gemm(bias=MISALIGNED) == -3
-    assert _gemm(M=0, Y=P(0)) == 0
+@pytest.mark.parametrize("fn", ["svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu"])
+def test_gemm_argument_errors(fn):
+    g = functools.partial(_gemm, fn=fn)
+    assert g(N=200) == -2 and g(K=200) == -2 and g(M=-3) == -2
+    assert g(r=24) == -6
+    assert g(sT=3.0) == -7 and g(sT=float("inf")) == -7 and g(sT=0.0) == -7
+    assert g(sT=2.0 ** -101) == -7 and g(sT=2.0 ** 101) == -7
+    assert g(Y=P(0)) == -1
+    assert g(a=MISALIGNED) == -3 and g(bias=MISALIGNED) == -3
+    assert g(M=0, Y=P(0)) == 0
 
 
 def test_awq_argument_errors():
@@ -105,6 +110,7 @@ def test_awq_argument_errors():
 @pytest.mark.skipif(HAS_GPU, reason="valid arguments would launch on a real device")
 def test_device_calls_without_device_report_cuda_error():
     assert _qa() == -5 and _gemm() == -5 and _awq() == -5
+    assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5
 
 
 # ------------------------------------------------------------- host packers

@@ -276,3 +276,18 @@ def test_gelu_tanh_identities():
     assert svdq.gelu_tanh_bf16(np.array([0.0]))[0] == 0.0
     big = np.array([30.0, -30.0])
     assert svdq.gelu_tanh_bf16(big).tolist() == [30.0, -0.0]
+
+
+def test_gelu_tanh_matches_library_and_taylor():
+    """The constants of the tanh form: torch's own tanh-approximated GELU in
+    float64 (a library routine, not this code) agrees to rounding; and both
+    GELU forms share the expansion y/2 + y^2/sqrt(2 pi) + O(y^4), which fixes
+    the sqrt(2/pi) factor independently of any implementation."""
+    import torch
+    y = np.concatenate([np.linspace(-12, 12, 4801), [1e-30, -1e-30, 1e3, -1e3]])
+    ref = torch.nn.functional.gelu(torch.from_numpy(y), approximate="tanh").numpy()
+    assert np.max(np.abs(svdq.gelu_tanh(y) - ref) / (1.0 + np.abs(y))) < 1e-14
+    # (g(h) - h/2) / h^2 = c/2 + (c a - c^3/3) h^2 / 2 + ..., |that h^2 term| < 0.07 h^2
+    for h in (1e-3, 1e-4):
+        second = (svdq.gelu_tanh(np.array([h]))[0] - h / 2) / h ** 2
+        assert abs(second - 1 / np.sqrt(2 * np.pi)) < h ** 2
