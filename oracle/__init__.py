@@ -1,4 +1,6 @@
-"""CPU oracle for the SVDQuant W4A4 (NVFP4) linear layer and the AWQ W4A16 GEMV.
+"""CPU oracle for the SVDQuant W4A4 (NVFP4) linear layer and the AWQ W4A16 GEMV,
+and for the epilogues fused onto the linear (GELU of an MLP's first linear;
+normalization and rotary embedding of a fused QKV projection, ``qkv``).
 
 TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the package-level
 smoke check and the benchmark's CPU-baseline leg may import or call anything in

@@ -139,3 +139,46 @@ def make_awq_weights(block: int, N: int = AWQ_N, K: int = AWQ_K, seed: int = AWQ
     W = rng_w.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)
     bias = to_bf16_values(rng_b.standard_normal(N, dtype=np.float32) * np.float32(0.01))
     return W, bias
+
+
+# ---------------------------------------------------------------------------
+# Fused QKV epilogue (normalization of Q and K, rotary embedding)
+# ---------------------------------------------------------------------------
+
+QKV_TEXT_TOKENS = 512           # the qkv case: 512 text tokens, then 64 x 64 image patches
+QKV_GRID = (64, 64)
+ROPE_AXES = (16, 56, 56)        # channels of a 128-wide head given to each position axis
+ROPE_BASE = 10000.0
+QKV_NORM_SEED = 5
+
+
+def rope_positions(n_text: int = QKV_TEXT_TOKENS, grid=QKV_GRID) -> np.ndarray:
+    """[M, 3] integer positions of the tokens: the text tokens first, all at
+    (0, 0, 0), then the image patches in row-major order at (0, row, col)."""
+    gh, gw = grid
+    img = np.zeros((gh * gw, 3), dtype=np.int64)
+    img[:, 1] = np.repeat(np.arange(gh), gw)
+    img[:, 2] = np.tile(np.arange(gw), gh)
+    return np.concatenate([np.zeros((n_text, 3), dtype=np.int64), img])
+
+
+def make_rope_tables(positions: np.ndarray, axes=ROPE_AXES, base: float = ROPE_BASE):
+    """(cos, sin) [M, sum(axes)/2] float32 rotary tables (input data of the
+    fused epilogue): the channel pairs of a head are split over the position
+    axes in order, and pair j of an axis with d channels turns by
+    position * base^(-2j/d) (the rotary embedding's frequency ladder, per axis)."""
+    positions = np.asarray(positions, dtype=np.float64)
+    angles = []
+    for a, d in enumerate(axes):
+        freq = base ** (-np.arange(0, d, 2, dtype=np.float64) / d)
+        angles.append(positions[:, a:a + 1] * freq[None, :])
+    theta = np.concatenate(angles, axis=1)
+    return np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+
+
+def make_qk_norm_weights(head_dim: int = 128, seed: int = QKV_NORM_SEED):
+    """(w_q, w_k) [head_dim] bf16 values ~ 1 + N(0, 0.1^2): the learned scales
+    of the Q and K normalizations."""
+    rq, rk = _streams(seed, 2)
+    return tuple(to_bf16_values(1.0 + 0.1 * r.standard_normal(head_dim, dtype=np.float32))
+                 for r in (rq, rk))
