@@ -163,6 +163,26 @@ def _check_cuda(t, name):
             raise ValueError(f"{name} must be a CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous (the library reads raw row-major memory)")
+        cur = _torch().cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}; the library runs on the current device "
+                             f"(cuda:{cur})")
+
+
+_WIDTH = {1: "8-bit", 2: "16-bit", 4: "32-bit"}
+
+
+def _need(t, name: str, elems: int, size: int):
+    """The kernels read or write `elems` elements of `size` bytes through t's
+    pointer: refuse a tensor of another element width or fewer elements (a
+    short buffer would be overrun on the device).  An empty need checks
+    nothing (no byte of t is touched)."""
+    if t is None or elems <= 0:
+        return
+    if t.element_size() != size:
+        raise ValueError(f"{name}: {_WIDTH[size]} elements expected, got {t.dtype}")
+    if t.numel() < elems:
+        raise ValueError(f"{name}: {elems} elements needed, the tensor holds {t.numel()}")
 
 
 def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None,
@@ -170,7 +190,8 @@ def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None
     """X: CUDA bf16 (or int16/uint16 bits) [M, K]; inv_lambda fp32 [K];
     L1s bf16 bits [rank, K].  Returns (a_codes, a_scales, lora_act)."""
     torch = _torch()
-    for t, n in ((X, "X"), (inv_lambda, "inv_lambda"), (L1s, "L1s")):
+    for t, n in ((X, "X"), (inv_lambda, "inv_lambda"), (L1s, "L1s"), (a_codes, "a_codes"),
+                 (a_scales, "a_scales"), (lora_act, "lora_act"), (dev_status, "dev_status")):
         _check_cuda(t, n)
     M, K = X.shape
     dev = X.device
@@ -180,6 +201,12 @@ def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None
         a_scales = torch.empty(scale_bytes(M, K), dtype=torch.uint8, device=dev)
     if lora_act is None:
         lora_act = torch.empty((M, rank), dtype=torch.bfloat16, device=dev)
+    if M > 0:
+        for t, n, e, z in ((X, "X", M * K, 2), (inv_lambda, "inv_lambda", K, 4),
+                           (L1s, "L1s", rank * K, 2), (a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", scale_bytes(M, K), 1),
+                           (lora_act, "lora_act", M * rank, 2), (dev_status, "dev_status", 1, 4)):
+            _need(t, n, e, z)
     st = _lib.svdq_quantize_act(_dptr(X), _dptr(inv_lambda), _dptr(L1s), M, K, int(rank),
                                 _dptr(a_codes), _dptr(a_scales), _dptr(lora_act),
                                 _dptr(dev_status), _stream_ptr(stream))
@@ -191,10 +218,20 @@ def _gemm(name, a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, 
           N, K, rank, Y, dev_status, stream):
     torch = _torch()
     for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
-                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias")):
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias"),
+                 (Y, "Y"), (dev_status, "dev_status")):
         _check_cuda(t, n)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    if M > 0:
+        for t, n, e, z in ((a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", scale_bytes(M, K), 1),
+                           (w_codes, "w_codes", code_bytes(N, K), 1),
+                           (w_scales, "w_scales", scale_bytes(N, K), 1),
+                           (lora_act, "lora_act", M * rank, 2), (L2s, "L2s", N * rank, 2),
+                           (bias, "bias", N, 2), (Y, "Y", M * N, 2),
+                           (dev_status, "dev_status", 1, 4)):
+            _need(t, n, e, z)
     st = getattr(_lib, name)(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales),
                              float(w_tensor_scale), _dptr(lora_act), _dptr(L2s), _dptr(bias),
                              _dptr(Y), int(M), int(N), int(K), int(rank), _dptr(dev_status),
@@ -225,12 +262,17 @@ def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None
     """X: CUDA bf16 [M, K] (M <= 8); returns Y [M, N] bf16."""
     torch = _torch()
     for t, n in ((X, "X"), (qweight, "qweight"), (scales, "scales"), (zeros, "zeros"),
-                 (bias, "bias")):
+                 (bias, "bias"), (Y, "Y"), (dev_status, "dev_status")):
         _check_cuda(t, n)
     M, K = X.shape
     N = qweight.shape[0]
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    groups = K // group_size if group_size > 0 else 0
+    for t, n, e, z in ((X, "X", M * K, 2), (qweight, "qweight", N * K // 2, 1),
+                       (scales, "scales", N * groups, 2), (zeros, "zeros", N * groups, 2),
+                       (bias, "bias", N, 2), (Y, "Y", M * N, 2), (dev_status, "dev_status", 1, 4)):
+        _need(t, n, e, z)
     st = _lib.awq_gemv_w4a16(_dptr(X), _dptr(qweight), _dptr(scales), _dptr(zeros), _dptr(bias),
                              _dptr(Y), int(M), int(N), int(K), int(group_size),
                              _dptr(dev_status), _stream_ptr(stream))

@@ -210,3 +210,20 @@ def test_awq_packer_errors():
         lib.awq_pack_weights(np.zeros((4, 100), np.float32))
     with pytest.raises(lib.SvdqError):
         lib.awq_pack_weights(np.full((4, 64), np.inf, np.float32))
+
+
+# ------------------------------------------------------------- binding buffer checks
+def test_binding_refuses_short_or_mistyped_buffers():
+    """The binding's size guard (a short buffer would be overrun on the device):
+    element width and element count, checked on host tensors without a call."""
+    from bit_w4a4_diffusion_quantize_b300 import _lib as b
+    b._need(torch.zeros(8, dtype=torch.int16), "x", 8, 2)
+    b._need(torch.zeros(8, dtype=torch.bfloat16), "x", 8, 2)
+    b._need(None, "bias", 8, 2)                                   # nullable
+    b._need(torch.zeros(0, dtype=torch.uint8), "lora", 0, 2)      # nothing touched: no check
+    with pytest.raises(ValueError, match="8 elements needed"):
+        b._need(torch.zeros(7, dtype=torch.int16), "x", 8, 2)
+    with pytest.raises(ValueError, match="16-bit elements expected"):
+        b._need(torch.zeros(8, dtype=torch.float32), "x", 8, 2)
+    with pytest.raises(ValueError, match="8-bit elements expected"):
+        b._need(torch.zeros(8, dtype=torch.int16), "codes", 8, 1)
