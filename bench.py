@@ -418,7 +418,93 @@ def run_gpu(args, world, rank, local):
         mlp = run_mlp_gelu(args, lib, dev, stream, world)
         line["mlp_fc1_gelu"] = mlp
         line["gpu_launches"] += mlp["launches"]
+    if not args.no_qkv_epilogue:
+        qk = run_qkv_epilogue(args, lib, dev, stream, world)
+        line["qkv_norm_rope"] = qk
+        line["gpu_launches"] += qk["launches"]
     return line
+
+
+def _time_graph(args, launch, fn, stream, dev, world):
+    """Per-launch seconds of `args.steps` launches of fn captured in a CUDA
+    graph (eager warm-up first), max over ranks."""
+    import torch
+    for i in range(args.warmup):
+        launch(fn, i, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream(dev)
+        for i in range(args.steps):
+            launch(fn, i, cs)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world, dev)
+
+
+def run_qkv_epilogue(args, lib, dev, stream, world):
+    """The fused QKV projection (M = 4608 tokens: 512 text + 4096 image,
+    K = 3072, N = 9216 = 3 x 24 heads x 128, rank 32) with the per-head RMS
+    normalization of Q and K and the rotary embedding in the GEMM epilogue
+    (svdq_gemm_w4a4_qkv), against the plain GEMM on the same operands.
+    Unfused, normalization and rotation would read and write the Q and K
+    columns once more each (2 x 2 x M x 2N/3 x 2 bytes)."""
+    import torch
+    case = workloads.CASES["qkv"]
+    M, K, N, r = case.M, case.K, case.N, case.rank
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    Xbits = workloads.bf16_bits_of(X)
+    packed = lib.svdq_pack_weights(W, lib.svdq_calib_absmax(Xbits), r)
+    nq, nk = workloads.make_qk_norm_weights()
+    cos, sin = workloads.make_rope_tables(workloads.rope_positions())
+
+    def dbits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sets = []
+    for _ in range(3):        # three weight + output sets (> 3 x L2 in all), rotated
+        s = {"wc": torch.from_numpy(packed["w_codes"]).to(dev),
+             "ws": torch.from_numpy(packed["w_scales"]).to(dev),
+             "L2s": dbits(packed["L2s"]), "bias": dbits(workloads.bf16_bits_of(b)),
+             "Y": torch.empty((M, N), dtype=torch.bfloat16, device=dev)}
+        s["ac"], s["as"], s["lora"] = lib.svdq_quantize_act(
+            dbits(Xbits).view(M, K), torch.from_numpy(packed["inv_lambda"]).to(dev),
+            dbits(packed["L1s"]), r, dev_status=status, stream=stream)
+        sets.append(s)
+    nq_d, nk_d = dbits(workloads.bf16_bits_of(nq)), dbits(workloads.bf16_bits_of(nk))
+    cos_d, sin_d = torch.from_numpy(cos).to(dev), torch.from_numpy(sin).to(dev)
+
+    def plain(s, st):
+        lib.svdq_gemm_w4a4(s["ac"], s["as"], s["wc"], s["ws"], packed["w_tensor_scale"],
+                           s["lora"], s["L2s"], s["bias"], M, N, K, r, s["Y"],
+                           dev_status=status, stream=st)
+
+    def fused(s, st):
+        lib.svdq_gemm_w4a4_qkv(s["ac"], s["as"], s["wc"], s["ws"], packed["w_tensor_scale"],
+                               s["lora"], s["L2s"], s["bias"], nq_d, nk_d, cos_d, sin_d, M, N,
+                               K, r, QKV=s["Y"], dev_status=status, stream=st)
+
+    def launch(fn, i, st):
+        fn(sets[i % len(sets)], st)
+
+    res = {"workload": f"qkv: SVDQ W4A4 linear + Q/K RMS norm + rotary M={M} K={K} N={N} "
+                       f"rank={r}", "launches": 2 * args.steps}
+    for name, fn in (("fused", fused), ("plain", plain)):
+        t = _time_graph(args, launch, fn, stream, dev, world)
+        res[f"us_{name}"] = round(t * 1e6, 2)
+        res[f"tflops_{name}"] = round(world * 2.0 * M * N * K / t / 1e12, 1)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the QKV epilogue phase")
+    res["epilogue_cost"] = round(res["us_fused"] / res["us_plain"] - 1.0, 4)
+    res["separate_pass_bytes_avoided"] = 2 * 2 * M * (2 * N // 3) * 2
+    return res
 
 
 def run_mlp_gelu(args, lib, dev, stream, world):
@@ -569,6 +655,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mlp-gelu", action="store_true",
                     help="skip the fc1 + fused GELU phase")
+    ap.add_argument("--no-qkv-epilogue", action="store_true",
+                    help="skip the QKV + normalization + rotary phase")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of repeated steps (untimed) over which clocks are sampled")
     args = ap.parse_args(argv)

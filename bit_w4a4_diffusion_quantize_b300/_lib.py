@@ -48,6 +48,8 @@ _SIGS = {
                               _i32, _i32, _i32, _c_p, _c_p]),
     "svdq_gemm_w4a4_gelu": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p,
                                    _i32, _i32, _i32, _i32, _c_p, _c_p]),
+    "svdq_gemm_w4a4_qkv": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                  _c_p, _c_p, _f32, _c_p, _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
@@ -255,6 +257,31 @@ def svdq_gemm_w4a4_gelu(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: fl
     H = bf16(gelu_tanh(Y)) [M, N] (CUDA)."""
     return _gemm("svdq_gemm_w4a4_gelu", a_codes, a_scales, w_codes, w_scales, w_tensor_scale,
                  lora_act, L2s, bias, M, N, K, rank, H, dev_status, stream)
+
+
+def svdq_gemm_w4a4_qkv(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float, lora_act,
+                       L2s, bias, norm_q, norm_k, rope_cos, rope_sin, M: int, N: int, K: int,
+                       rank: int, eps: float = 1e-6, QKV=None, dev_status=None, stream=None):
+    """svdq_gemm_w4a4 of a fused Q|K|V projection (N = 3 x heads x 128) with the
+    per-head RMS normalization of Q and K (weights norm_q, norm_k: [128] bf16)
+    and the rotary embedding (rope_cos, rope_sin: [M, 64] fp32) in its
+    epilogue.  Returns QKV [M, N] bf16 (CUDA)."""
+    torch = _torch()
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias"),
+                 (norm_q, "norm_q"), (norm_k, "norm_k"), (rope_cos, "rope_cos"),
+                 (rope_sin, "rope_sin")):
+        _check_cuda(t, n)
+    if QKV is None:
+        QKV = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    st = _lib.svdq_gemm_w4a4_qkv(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes),
+                                 _dptr(w_scales), float(w_tensor_scale), _dptr(lora_act),
+                                 _dptr(L2s), _dptr(bias), _dptr(norm_q), _dptr(norm_k),
+                                 _dptr(rope_cos), _dptr(rope_sin), float(eps), _dptr(QKV),
+                                 int(M), int(N), int(K), int(rank), _dptr(dev_status),
+                                 _stream_ptr(stream))
+    _check(st, "svdq_gemm_w4a4_qkv")
+    return QKV
 
 
 def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None,

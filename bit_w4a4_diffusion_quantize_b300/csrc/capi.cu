@@ -177,9 +177,13 @@ namespace {
 svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
                       const uint8_t* w_scales, float w_tensor_scale, const uint16_t* lora_act,
                       const uint16_t* L2s, const uint16_t* bias, uint16_t* Y, int M, int N,
-                      int K, int rank, bool gelu, int* dev_status, void* stream) {
+                      int K, int rank, svdq::GemmEpilogue epi, const svdq::QkvEpilogue& qe,
+                      int* dev_status, void* stream) {
+  const bool is_qkv = epi == svdq::GemmEpilogue::kQkv;
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (is_qkv && N % 768 != 0) return SVDQ_ERR_SHAPE;  // Q, K, V: whole pairs of 128-wide heads
   if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  if (is_qkv && !(std::isfinite(qe.eps) && qe.eps >= 0.0f)) return SVDQ_ERR_VALUE;
   {
     // a finite power of two in [2^-100, 2^100]
     int ex = 0;
@@ -190,9 +194,14 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
   if (M == 0) return SVDQ_OK;
   if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2s || !Y)
     return SVDQ_ERR_NULL;
+  if (is_qkv && (!qe.norm_q || !qe.norm_k || !qe.rope_cos || !qe.rope_sin))
+    return SVDQ_ERR_NULL;
   if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
       !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2s) || !aligned16(Y) ||
       (bias && !aligned16(bias)))
+    return SVDQ_ERR_ALIGN;
+  if (is_qkv && (!aligned16(qe.norm_q) || !aligned16(qe.norm_k) || !aligned16(qe.rope_cos) ||
+                 !aligned16(qe.rope_sin)))
     return SVDQ_ERR_ALIGN;
   int sms = 0;
   svdq_status st = current_device(nullptr, &sms);
@@ -209,8 +218,8 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
   const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
   const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
-                                         bias, Y, M, N, K, rank, gelu, dev_status, test_stall,
-                                         sms, static_cast<cudaStream_t>(stream));
+                                         bias, Y, M, N, K, rank, epi, qe, dev_status,
+                                         test_stall, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 
@@ -224,7 +233,8 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
                            const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
                            int* dev_status, void* stream) {
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, Y,
-                   M, N, K, rank, false, dev_status, stream);
+                   M, N, K, rank, svdq::GemmEpilogue::kPlain, svdq::QkvEpilogue{}, dev_status,
+                   stream);
 }
 
 svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
@@ -233,7 +243,21 @@ svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
                                 const uint16_t* L2s, const uint16_t* bias, uint16_t* H, int M,
                                 int N, int K, int rank, int* dev_status, void* stream) {
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, H,
-                   M, N, K, rank, true, dev_status, stream);
+                   M, N, K, rank, svdq::GemmEpilogue::kGelu, svdq::QkvEpilogue{}, dev_status,
+                   stream);
+}
+
+svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,
+                               const uint8_t* w_codes, const uint8_t* w_scales,
+                               float w_tensor_scale, const uint16_t* lora_act,
+                               const uint16_t* L2s, const uint16_t* bias,
+                               const uint16_t* norm_q, const uint16_t* norm_k,
+                               const float* rope_cos, const float* rope_sin, float eps,
+                               uint16_t* QKV, int M, int N, int K, int rank, int* dev_status,
+                               void* stream) {
+  const svdq::QkvEpilogue qe{norm_q, norm_k, rope_cos, rope_sin, eps, N / 3};
+  return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias,
+                   QKV, M, N, K, rank, svdq::GemmEpilogue::kQkv, qe, dev_status, stream);
 }
 
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

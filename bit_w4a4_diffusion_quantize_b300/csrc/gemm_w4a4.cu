@@ -12,6 +12,10 @@
 //                                             linear of a transformer MLP
 //                                             (dothoosh.com, same article: the
 //                                             full engine's GELU/MLP kernels)
+//   or the QKV variant: Y's Q and K heads (128 columns each) RMS-normalized
+//      and turned pair by pair by the tokens' rotary angles, V as Y (same
+//      article, structural rewrites: one fused operator for the QKV
+//      projection, the Q/K normalization and the rotary embeddings)
 //
 // Persistent kernel in clusters of two CTAs (one CTA per SM).  A cluster walks
 // pairs of 128 x BN output tiles that share their columns (BN = 256, or 128
@@ -44,7 +48,10 @@
 //              lane, BN/4 columns each): one tcgen05.ld of their columns, and
 //              `acc_empty` is released at once -- the single accumulator is
 //              held only for that load; then y = s_T * acc + bias rounded to
-//              bf16 pairs, and an 8 x 8 (4 x 4 at BN = 128) transpose of
+//              bf16 pairs (QKV: the two warps holding the halves of a head
+//              swap their rows' partial sums of squares through shared memory
+//              behind a two-warp barrier, then normalize and rotate), and an
+//              8 x 8 (4 x 4 at BN = 128) transpose of
 //              16-byte chunks inside groups of lanes (warp shuffles) turns
 //              "one row per lane" into "8 lanes per row": each store
 //              instruction writes 4 whole 128-byte row segments.
@@ -82,7 +89,12 @@ constexpr int SMEM_BUDGET = 224 * 1024;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
-template <int BN, int RANK>
+// epilogue kinds: bf16 Y; bf16 gelu_tanh(Y); Y with its Q and K heads
+// RMS-normalized and rotated (fused QKV projection)
+constexpr int kEpiPlain = 0, kEpiGelu = 1, kEpiQkv = 2;
+constexpr int kHeadDim = 128;  // QKV epilogue: channels of one head
+
+template <int BN, int RANK, int EPI>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK_BYTES;
   static constexpr int B_BYTES = BN * BK_BYTES;
@@ -95,16 +107,22 @@ struct Cfg {
   static_assert(LA_BYTES <= A_BYTES && LB_BYTES <= B_BYTES, "rank-r operands fit a ring slot");
   static constexpr int BIAS_BYTES = BN * 2;
   static constexpr int MISC_BYTES = 512;
-  static constexpr int FIXED_BYTES = 2 * BIAS_BYTES + MISC_BYTES;
+  // QKV: per-lane partial sums of squares exchanged by the two warps of a head
+  // (two buffers), and one barrier per warp pair
+  static constexpr int XSUM_BYTES = EPI == kEpiQkv ? 2 * 16 * 32 * 4 : 0;
+  static constexpr int PAIR_BARS = EPI == kEpiQkv ? 8 : 0;
+  static constexpr int FIXED_BYTES = 2 * BIAS_BYTES + XSUM_BYTES + MISC_BYTES;
   static constexpr int STAGES = cmin(6, (SMEM_BUDGET - 1024 - FIXED_BYTES) / STAGE_BYTES);
   static constexpr int OFF_A = 0;  // slot areas 1024-aligned (swizzle atoms)
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_BIAS = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_BIAS + 2 * BIAS_BYTES;
-  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full, acc_empty
-  static constexpr int NUM_BARS = 3 * STAGES + 4;
+  static constexpr int OFF_XSUM = OFF_BIAS + 2 * BIAS_BYTES;
+  static constexpr int OFF_BAR = OFF_XSUM + XSUM_BYTES;
+  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full, acc_empty,
+  // pair[PAIR_BARS]
+  static constexpr int NUM_BARS = 3 * STAGES + 4 + PAIR_BARS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + base alignment slack
   // TMEM columns: accumulator [0, BN), then per stage the scales of A and B
@@ -194,6 +212,42 @@ SVDQ_DEVINL void pack_cols32(const uint32_t* v, float s_T, const uint16_t* bias,
   }
 }
 
+// QKV epilogue for one lane's 64 columns of one head: 32 bf16 pairs in v[0..31]
+// (head channels 2 p0 .. 2 p0 + 63 of token `row`; w: the weights of those
+// channels).  n = (y * rs) * w (RMS normalization with rs = 1/sqrt(mean + eps)),
+// then channel pair (a, b) turned by the token's angle: (a cos - b sin,
+// a sin + b cos); rounded to bf16 pairs in place.
+SVDQ_DEVINL void qkv_norm_rotate(uint32_t* v, float rs, const uint16_t* w, const float* rope_cos,
+                                 const float* rope_sin, int row, int p0) {
+  const float* cs = rope_cos + (size_t)row * (kHeadDim / 2) + p0;
+  const float* sn = rope_sin + (size_t)row * (kHeadDim / 2) + p0;
+  // one chunk of 4 pairs per iteration, not unrolled (so that the table loads
+  // of later chunks are not all held in registers at once); the chunk is
+  // always v[0..3]: the 32 pairs rotate down by 4 each iteration and are back
+  // in place after 8
+#pragma unroll 1
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const uint4 ww = __ldg(reinterpret_cast<const uint4*>(w) + c4);  // 8 weights, 4 pairs
+    const float4 co = __ldg(reinterpret_cast<const float4*>(cs) + c4);
+    const float4 si = __ldg(reinterpret_cast<const float4*>(sn) + c4);
+    const uint32_t wp[4] = {ww.x, ww.y, ww.z, ww.w};
+    const float cc[4] = {co.x, co.y, co.z, co.w}, sv[4] = {si.x, si.y, si.z, si.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = (bf16lo_to_f32(v[i]) * rs) * bf16lo_to_f32(wp[i]);
+      const float b = (bf16hi_to_f32(v[i]) * rs) * bf16hi_to_f32(wp[i]);
+      const __nv_bfloat162 o = __floats2bfloat162_rn(__fmaf_rn(a, cc[i], -(b * sv[i])),
+                                                     __fmaf_rn(a, sv[i], b * cc[i]));
+      out[i] = *reinterpret_cast<const uint32_t*>(&o);
+    }
+#pragma unroll
+    for (int i = 0; i < 28; ++i) v[i] = v[i + 4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[28 + i] = out[i];
+  }
+}
+
 // Inside each group of CH lanes (CH = 8 or 4), transpose the CH x CH matrix of
 // 16-byte chunks (lane = row, chunk index = column): afterwards chunk i of
 // lane t holds what was chunk t % CH of lane (t & ~(CH-1)) + i.  log2(CH)
@@ -217,15 +271,16 @@ SVDQ_DEVINL void transpose_chunks(uint32_t (&c)[4 * CH], int lane) {
   }
 }
 
-template <int BN, int RANK, bool GELU>
+template <int BN, int RANK, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_w4a4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_lora,
                 const __grid_constant__ CUtensorMap tm_l2s, const uint8_t* __restrict__ a_scales,
                 const uint8_t* __restrict__ w_scales, float s_T,
                 const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
-                int* dev_status, int test_stall, uint64_t wait_ns) {
-  using C = Cfg<BN, RANK>;
+                const QkvEpilogue qe, int* dev_status, int test_stall, uint64_t wait_ns) {
+  static_assert(EPI != kEpiQkv || BN == 2 * kHeadDim, "QKV epilogue: two heads per tile");
+  using C = Cfg<BN, RANK, EPI>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -236,6 +291,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bias_empty = sf_full + STAGES;  // [2]
   uint64_t* acc_full = bias_empty + 2;
   uint64_t* acc_empty = acc_full + 1;
+  uint64_t* pair_bar = acc_empty + 1;  // [PAIR_BARS]
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
   volatile uint32_t* abort_flag = &misc[1];
 
@@ -266,6 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&bias_empty[1], EPI_WARPS);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, EPI_WARPS * 32);
+    for (int b = 0; b < C::PAIR_BARS; ++b) mbar_init(&pair_bar[b], 2);
     misc[1] = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
@@ -455,6 +512,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int col0 = ((warp - EPI_WARP0) >> 2) * C::EPI_COLS;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     const int gbase = lane & ~(CH - 1), tc = lane & (CH - 1);
+    // QKV: warps e and e ^ 4 hold the two 64-column halves of one head for the
+    // same 32 rows; `pid` names the pair, `qk` counts its exchanges
+    const int e = warp - EPI_WARP0;
+    const int pid = ((e >> 3) << 2) | (e & 3);
+    int qk = 0;
     for (int j = 0; j < my_tiles; ++j) {
       int m_tile, n_tile;
       tile_mn(j, m_tile, n_tile);
@@ -485,11 +547,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // bf16 pairs in place: pair i lands in v[i] (read from v[2i], v[2i+1])
 #pragma unroll
       for (int c = 0; c < C::EPI_COLS / 32; ++c)
-        pack_cols32<GELU>(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr, &v[16 * c]);
+        pack_cols32<EPI == kEpiGelu>(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr,
+                                     &v[16 * c]);
       uint32_t(&pk)[4 * CH] = *reinterpret_cast<uint32_t(*)[4 * CH]>(&v[0]);
       if (bsm) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bias_empty[j & 1]);
+      }
+      if constexpr (EPI == kEpiQkv) {
+        const int region = n0 < qe.hd ? 0 : (n0 < 2 * qe.hd ? 1 : 2);  // Q, K, V tile
+        if (region < 2) {
+          // sum of squares of this lane's 64 bf16 values (column order); the
+          // partner's half arrives through shared memory
+          float ss = 0.0f;
+#pragma unroll
+          for (int i = 0; i < C::EPI_COLS / 2; ++i) {
+            const float a = bf16lo_to_f32(v[i]), b = bf16hi_to_f32(v[i]);
+            ss = __fmaf_rn(a, a, ss);
+            ss = __fmaf_rn(b, b, ss);
+          }
+          float* xs = reinterpret_cast<float*>(smem + C::OFF_XSUM) + (qk & 1) * EPI_WARPS * 32;
+          xs[e * 32 + lane] = ss;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pair_bar[pid]);
+          const bool got =
+              mbar_wait(&pair_bar[pid], (uint32_t)(qk & 1), dev_status, wait_ns) && !*abort_flag;
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            *abort_flag = 1;
+            break;
+          }
+          ++qk;
+          const float other = xs[(e ^ 4) * 32 + lane];
+          const float total = (e & 4) ? other + ss : ss + other;  // lower columns first
+          const float rs = rsqrtf(__fmaf_rn(total, 1.0f / kHeadDim, qe.eps));
+          qkv_norm_rotate(v, rs, (region == 0 ? qe.norm_q : qe.norm_k) + (col0 & (kHeadDim - 1)),
+                          qe.rope_cos, qe.rope_sin, min(m0 + 32 * q + lane, M - 1),
+                          (col0 & (kHeadDim - 1)) >> 1);
+        }
       }
       // after the transpose, store i of lane t writes chunk t % CH of row
       // (t & ~(CH-1)) + i: CH consecutive lanes cover one row segment
@@ -522,12 +616,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, int RANK, bool GELU>
+template <int BN, int RANK, int EPI>
 cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
                      float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
-                     int* dev_status, int test_stall, int num_sms, cudaStream_t stream) {
-  using C = Cfg<BN, RANK>;
-  auto kern = k_gemm_w4a4<BN, RANK, GELU>;
+                     const QkvEpilogue& qe, int* dev_status, int test_stall, int num_sms,
+                     cudaStream_t stream) {
+  using C = Cfg<BN, RANK, EPI>;
+  auto kern = k_gemm_w4a4<BN, RANK, EPI>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -562,24 +657,43 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, maps.a_codes, maps.w_codes, maps.lora, maps.l2s, a_scales,
-                         w_scales, s_T, bias, Y, M, N, K, dev_status, test_stall,
+                         w_scales, s_T, bias, Y, M, N, K, qe, dev_status, test_stall,
                          (uint64_t)(test_stall ? 100000000ull : kWaitTimeoutNs));
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// the QKV epilogue exists for two-head tiles only (block_n 256)
+template <int BN, int RANK>
+cudaError_t launch_qkv_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
+                         float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                         const QkvEpilogue& qe, int* dev_status, int test_stall, int num_sms,
+                         cudaStream_t stream) {
+  if constexpr (BN == 2 * kHeadDim)
+    return launch_t<BN, RANK, kEpiQkv>(maps, a_scales, w_scales, s_T, bias, Y, M, N, K, qe,
+                                       dev_status, test_stall, num_sms, stream);
+  else
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
-                             uint16_t* Y, int M, int N, int K, int rank, bool gelu,
-                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream) {
+                             uint16_t* Y, int M, int N, int K, int rank, GemmEpilogue epi,
+                             const QkvEpilogue& qe, int* dev_status, int test_stall,
+                             int num_sms, cudaStream_t stream) {
+#define SVDQ_GEMM_LAUNCH(BN_, R_, E_)                                                        \
+  return launch_t<BN_, R_, E_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N, K,   \
+                               qe, dev_status, test_stall, num_sms, stream)
 #define SVDQ_GEMM_CASE(BN_, R_)                                                              \
-  if (block_n == BN_ && rank == R_)                                                          \
-    return gelu ? launch_t<BN_, R_, true>(maps, a_scales, w_scales, w_tensor_scale, bias, Y,  \
-                                          M, N, K, dev_status, test_stall, num_sms, stream)  \
-                : launch_t<BN_, R_, false>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, \
-                                           M, N, K, dev_status, test_stall, num_sms, stream);
+  if (block_n == BN_ && rank == R_) {                                                        \
+    if (epi == GemmEpilogue::kPlain) SVDQ_GEMM_LAUNCH(BN_, R_, kEpiPlain);                   \
+    if (epi == GemmEpilogue::kGelu) SVDQ_GEMM_LAUNCH(BN_, R_, kEpiGelu);                     \
+    if (epi == GemmEpilogue::kQkv)                                                           \
+      return launch_qkv_t<BN_, R_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N,  \
+                                   K, qe, dev_status, test_stall, num_sms, stream);          \
+  }
   SVDQ_GEMM_CASE(256, 16)
   SVDQ_GEMM_CASE(256, 32)
   SVDQ_GEMM_CASE(256, 64)
@@ -587,6 +701,7 @@ cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a
   SVDQ_GEMM_CASE(128, 32)
   SVDQ_GEMM_CASE(128, 64)
 #undef SVDQ_GEMM_CASE
+#undef SVDQ_GEMM_LAUNCH
   return cudaErrorInvalidValue;
 }
 

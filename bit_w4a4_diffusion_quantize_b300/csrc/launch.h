@@ -23,10 +23,26 @@ struct GemmMaps {
   CUtensorMap l2s;      // L2s [N][rank] bf16: box rank x BN rows, same swizzle
 };
 
+// What svdq_gemm_w4a4's epilogue does after y = s_T * acc + bias is rounded to
+// bf16: nothing; GELU (tanh form); per-head RMS normalization and rotary
+// embedding of the Q and K column blocks (fused QKV projection, block_n 256).
+enum class GemmEpilogue { kPlain, kGelu, kQkv };
+
+// Operands of the QKV epilogue (all null / zero for the others).
+struct QkvEpilogue {
+  const uint16_t* norm_q;  // [128] bf16 weights of the Q normalization
+  const uint16_t* norm_k;  // [128] bf16 weights of the K normalization
+  const float* rope_cos;   // [M][64] fp32, per token and channel pair
+  const float* rope_sin;   // [M][64] fp32
+  float eps;               // added to the mean square
+  int hd;                  // columns of each of Q, K, V: N / 3 (a multiple of 256)
+};
+
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
-                             uint16_t* Y, int M, int N, int K, int rank, bool gelu,
-                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream);
+                             uint16_t* Y, int M, int N, int K, int rank, GemmEpilogue epi,
+                             const QkvEpilogue& qe, int* dev_status, int test_stall,
+                             int num_sms, cudaStream_t stream);
 
 // Largest K the AWQ GEMV stages in shared memory.
 int awq_max_k();

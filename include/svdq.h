@@ -227,6 +227,33 @@ svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
                                 int M, int N, int K, int rank, int* dev_status,
                                 void* stream);
 
+/* svdq_gemm_w4a4 for a fused Q|K|V projection, with the normalization of Q and
+ * K and the rotary embedding in its epilogue (dothoosh.com, "How Nunchaku Lite
+ * halves the VRAM of diffusion models", paragraphs on structural rewrites:
+ * to_q, to_k, to_v joined along the output dimension in the order Q, K, V, and
+ * one fused operator for the projection, the Q/K normalization and the rotary
+ * embeddings).  With Y_b the bf16 output svdq_gemm_w4a4 returns for the same
+ * arguments and heads of D = 128 columns:
+ *   V columns [2N/3, N):    QKV = Y_b
+ *   Q columns [0, N/3), K columns [N/3, 2N/3), per token m and head h:
+ *     n[c]  = Y_b[c] / sqrt( mean_c Y_b[c]^2 + eps ) * w[c]   (w = norm_q or norm_k)
+ *     (QKV[2i], QKV[2i+1]) = bf16( n[2i] cos - n[2i+1] sin, n[2i] sin + n[2i+1] cos ),
+ *     cos = rope_cos[m][i], sin = rope_sin[m][i], i = 0 .. 63 (the same for every head)
+ * evaluated in fp32 (relative error below 2^-16 of the pair's norm), rounded
+ * to nearest even once.
+ * Inputs: norm_q, norm_k [128] bf16; rope_cos, rope_sin [M][64] fp32 (16-byte
+ * aligned, caller-owned); eps >= 0 and finite (SVDQ_ERR_VALUE otherwise).
+ * Output: QKV [M][N] bf16.  Sizes: N % 768 == 0 (SVDQ_ERR_SHAPE otherwise);
+ * everything else as svdq_gemm_w4a4. */
+svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,
+                               const uint8_t* w_codes, const uint8_t* w_scales,
+                               float w_tensor_scale, const uint16_t* lora_act,
+                               const uint16_t* L2s, const uint16_t* bias,
+                               const uint16_t* norm_q, const uint16_t* norm_k,
+                               const float* rope_cos, const float* rope_sin, float eps,
+                               uint16_t* QKV, int M, int N, int K, int rank, int* dev_status,
+                               void* stream);
+
 /* AWQ W4A16 GEMV for the small-M modulation layers (kernel-family list:
  * memory-bound adaLN modulation):
  *   Y[m][n] = bf16( sum_k X[m][k] (q[n][k] - z[n][k/64]) s[n][k/64] + bias[n] )

@@ -36,7 +36,7 @@ def _declared_functions():
 def test_library_exports_every_declared_symbol():
     names = _declared_functions()
     assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu",
-            "awq_gemv_w4a16",
+            "svdq_gemm_w4a4_qkv", "awq_gemv_w4a16",
             "awq_pack_weights", "svdq_calib_absmax", "svdq_check_device",
             "svdq_status_string"} <= names
     raw = ctypes.CDLL(lib.LIB_PATH)
@@ -75,6 +75,13 @@ def _gemm(M=64, N=256, K=256, r=32, sT=2.0 ** -10, Y=ALIGNED, a=ALIGNED, bias=No
                                       ALIGNED, ALIGNED, bias, Y, M, N, K, r, None, None)
 
 
+def _qkv(M=64, N=768, K=256, r=32, eps=1e-6, nq=ALIGNED, cos=ALIGNED):
+    return lib.raw_lib().svdq_gemm_w4a4_qkv(ALIGNED, ALIGNED, ALIGNED, ALIGNED,
+                                            ctypes.c_float(2.0 ** -10), ALIGNED, ALIGNED, None,
+                                            nq, ALIGNED, cos, ALIGNED, ctypes.c_float(eps),
+                                            ALIGNED, M, N, K, r, None, None)
+
+
 def _awq(M=1, N=64, K=256, g=64, X=ALIGNED):
     return lib.raw_lib().awq_gemv_w4a16(X, ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, M, N, K, g,
                                         None, None)
@@ -100,6 +107,15 @@ def test_gemm_argument_errors(fn):
     assert g(M=0, Y=P(0)) == 0
 
 
+def test_qkv_argument_errors():
+    assert _qkv(N=512) == -2 and _qkv(N=1152) == -2      # not whole pairs of 128-wide heads
+    assert _qkv(r=8) == -6
+    assert _qkv(eps=-1e-6) == -7 and _qkv(eps=float("nan")) == -7 and _qkv(eps=float("inf")) == -7
+    assert _qkv(nq=P(0)) == -1 and _qkv(cos=P(0)) == -1
+    assert _qkv(cos=MISALIGNED) == -3 and _qkv(nq=MISALIGNED) == -3
+    assert _qkv(M=0, nq=P(0)) == 0
+
+
 def test_awq_argument_errors():
     assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(g=128) == -2
     assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
@@ -110,7 +126,7 @@ def test_awq_argument_errors():
 @pytest.mark.skipif(HAS_GPU, reason="valid arguments would launch on a real device")
 def test_device_calls_without_device_report_cuda_error():
     assert _qa() == -5 and _gemm() == -5 and _awq() == -5
-    assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5
+    assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5 and _qkv() == -5
 
 
 # ------------------------------------------------------------- host packers
