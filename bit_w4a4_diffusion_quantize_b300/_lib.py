@@ -270,10 +270,21 @@ def svdq_gemm_w4a4_qkv(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: flo
     for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
                  (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias"),
                  (norm_q, "norm_q"), (norm_k, "norm_k"), (rope_cos, "rope_cos"),
-                 (rope_sin, "rope_sin")):
+                 (rope_sin, "rope_sin"), (QKV, "QKV"), (dev_status, "dev_status")):
         _check_cuda(t, n)
     if QKV is None:
         QKV = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    if M > 0:
+        for t, n, e, z in ((a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", scale_bytes(M, K), 1),
+                           (w_codes, "w_codes", code_bytes(N, K), 1),
+                           (w_scales, "w_scales", scale_bytes(N, K), 1),
+                           (lora_act, "lora_act", M * rank, 2), (L2s, "L2s", N * rank, 2),
+                           (bias, "bias", N, 2), (norm_q, "norm_q", 128, 2),
+                           (norm_k, "norm_k", 128, 2), (rope_cos, "rope_cos", M * 64, 4),
+                           (rope_sin, "rope_sin", M * 64, 4), (QKV, "QKV", M * N, 2),
+                           (dev_status, "dev_status", 1, 4)):
+            _need(t, n, e, z)
     st = _lib.svdq_gemm_w4a4_qkv(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes),
                                  _dptr(w_scales), float(w_tensor_scale), _dptr(lora_act),
                                  _dptr(L2s), _dptr(bias), _dptr(norm_q), _dptr(norm_k),
