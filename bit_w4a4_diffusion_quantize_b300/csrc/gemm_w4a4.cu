@@ -212,39 +212,41 @@ SVDQ_DEVINL void pack_cols32(const uint32_t* v, float s_T, const uint16_t* bias,
   }
 }
 
-// QKV epilogue for one lane's 64 columns of one head: 32 bf16 pairs in v[0..31]
-// (head channels 2 p0 .. 2 p0 + 63 of token `row`; w: the weights of those
-// channels).  n = (y * rs) * w (RMS normalization with rs = 1/sqrt(mean + eps)),
-// then channel pair (a, b) turned by the token's angle: (a cos - b sin,
-// a sin + b cos); rounded to bf16 pairs in place.
-SVDQ_DEVINL void qkv_norm_rotate(uint32_t* v, float rs, const uint16_t* w, const float* rope_cos,
-                                 const float* rope_sin, int row, int p0) {
-  const float* cs = rope_cos + (size_t)row * (kHeadDim / 2) + p0;
-  const float* sn = rope_sin + (size_t)row * (kHeadDim / 2) + p0;
-  // one chunk of 4 pairs per iteration, not unrolled (so that the table loads
-  // of later chunks are not all held in registers at once); the chunk is
-  // always v[0..3]: the 32 pairs rotate down by 4 each iteration and are back
-  // in place after 8
+// QKV epilogue, after the 8 x 8 chunk transpose: lane t holds, for the 8 rows
+// row0 + i (i = 0..7, words pk[4i .. 4i+3]), the 8 columns 8 (t % 8) .. + 7 of
+// its warp's 64, i.e. the head channels whose weights start at w and the 4
+// channel pairs starting at pair p.  rs_lane is 1/rms of the row the lane held
+// before the transpose (row gbase + i comes by a shuffle).  n = (y * rs) * w,
+// then pair (a, b) turned by the token's angle: (a cos - b sin, a sin + b cos),
+// rounded to bf16 pairs in place.  The 8 lanes sharing a row read its table
+// slices side by side (128 contiguous bytes).  One row per iteration, not
+// unrolled, so that the table loads are not all held in registers at once:
+// the rows rotate through pk[0..3] and are back in place after 8.
+SVDQ_DEVINL void qkv_rotate_rows(uint32_t (&pk)[32], float rs_lane, int gbase, const uint16_t* w,
+                                 const float* rope_cos, const float* rope_sin, int row0, int M,
+                                 int p) {
+  const uint4 ww = __ldg(reinterpret_cast<const uint4*>(w));
+  const uint32_t wp[4] = {ww.x, ww.y, ww.z, ww.w};
 #pragma unroll 1
-  for (int c4 = 0; c4 < 8; ++c4) {
-    const uint4 ww = __ldg(reinterpret_cast<const uint4*>(w) + c4);  // 8 weights, 4 pairs
-    const float4 co = __ldg(reinterpret_cast<const float4*>(cs) + c4);
-    const float4 si = __ldg(reinterpret_cast<const float4*>(sn) + c4);
-    const uint32_t wp[4] = {ww.x, ww.y, ww.z, ww.w};
+  for (int i = 0; i < 8; ++i) {
+    const float rs = __shfl_sync(0xFFFFFFFFu, rs_lane, gbase + i);
+    const size_t off = (size_t)min(row0 + i, M - 1) * (kHeadDim / 2) + p;
+    const float4 co = __ldg(reinterpret_cast<const float4*>(rope_cos + off));
+    const float4 si = __ldg(reinterpret_cast<const float4*>(rope_sin + off));
     const float cc[4] = {co.x, co.y, co.z, co.w}, sv[4] = {si.x, si.y, si.z, si.w};
     uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = (bf16lo_to_f32(v[i]) * rs) * bf16lo_to_f32(wp[i]);
-      const float b = (bf16hi_to_f32(v[i]) * rs) * bf16hi_to_f32(wp[i]);
-      const __nv_bfloat162 o = __floats2bfloat162_rn(__fmaf_rn(a, cc[i], -(b * sv[i])),
-                                                     __fmaf_rn(a, sv[i], b * cc[i]));
-      out[i] = *reinterpret_cast<const uint32_t*>(&o);
+    for (int j = 0; j < 4; ++j) {
+      const float a = (bf16lo_to_f32(pk[j]) * rs) * bf16lo_to_f32(wp[j]);
+      const float b = (bf16hi_to_f32(pk[j]) * rs) * bf16hi_to_f32(wp[j]);
+      const __nv_bfloat162 o = __floats2bfloat162_rn(__fmaf_rn(a, cc[j], -(b * sv[j])),
+                                                     __fmaf_rn(a, sv[j], b * cc[j]));
+      out[j] = *reinterpret_cast<const uint32_t*>(&o);
     }
 #pragma unroll
-    for (int i = 0; i < 28; ++i) v[i] = v[i + 4];
+    for (int k = 0; k < 28; ++k) pk[k] = pk[k + 4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[28 + i] = out[i];
+    for (int j = 0; j < 4; ++j) pk[28 + j] = out[j];
   }
 }
 
@@ -554,9 +556,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bias_empty[j & 1]);
       }
+      // QKV: 1/rms of this lane's row (before the transpose), used after it
+      float rs = 0.0f;
+      const int region = EPI == kEpiQkv ? (n0 < qe.hd ? 0 : (n0 < 2 * qe.hd ? 1 : 2)) : 2;
       if constexpr (EPI == kEpiQkv) {
-        const int region = n0 < qe.hd ? 0 : (n0 < 2 * qe.hd ? 1 : 2);  // Q, K, V tile
-        if (region < 2) {
+        if (region < 2) {  // a Q or K tile
           // sum of squares of this lane's 64 bf16 values (column order); the
           // partner's half arrives through shared memory
           float ss = 0.0f;
@@ -579,15 +583,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++qk;
           const float other = xs[(e ^ 4) * 32 + lane];
           const float total = (e & 4) ? other + ss : ss + other;  // lower columns first
-          const float rs = rsqrtf(__fmaf_rn(total, 1.0f / kHeadDim, qe.eps));
-          qkv_norm_rotate(v, rs, (region == 0 ? qe.norm_q : qe.norm_k) + (col0 & (kHeadDim - 1)),
-                          qe.rope_cos, qe.rope_sin, min(m0 + 32 * q + lane, M - 1),
-                          (col0 & (kHeadDim - 1)) >> 1);
+          rs = rsqrtf(__fmaf_rn(total, 1.0f / kHeadDim, qe.eps));
         }
       }
       // after the transpose, store i of lane t writes chunk t % CH of row
       // (t & ~(CH-1)) + i: CH consecutive lanes cover one row segment
       transpose_chunks<CH>(pk, lane);
+      if constexpr (EPI == kEpiQkv) {
+        if (region < 2)
+          qkv_rotate_rows(pk, rs, gbase,
+                          (region == 0 ? qe.norm_q : qe.norm_k) + (col0 & (kHeadDim - 1)) + 8 * tc,
+                          qe.rope_cos, qe.rope_sin, m0 + 32 * q + gbase, M,
+                          ((col0 & (kHeadDim - 1)) >> 1) + 4 * tc);
+      }
       const int cbase = n0 + col0 + 8 * tc;
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
