@@ -13,7 +13,9 @@ every step reads from HBM, not L2.
 The AWQ phase times the 57 stacked adaLN modulation GEMVs (K = 3072,
 N = 6 x 3072, M in {1, 2, 4}) back to back; the MLP phase times the MLP's
 first linear (M = 4096, K = 3072, N = 12288) with GELU fused into its epilogue
-against the same GEMM without it.
+against the same GEMM without it; the QKV phase times the fused QKV projection
+(M = 4608, K = 3072, N = 9216) with the per-head RMS normalization of Q and K
+and the rotary embedding in its epilogue against the plain GEMM.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 a bounded sample of the same workload instead.
