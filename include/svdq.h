@@ -19,6 +19,11 @@
  *     awq_w4a16 for the precision-sensitive, memory-bound modulation layers.
  *   - same page, hardware list: the loader checks the device's CUDA compute
  *     capability and raises a clear error instead of producing wrong output.
+ *   - same page, on the full engine's model-specific fused paths and its
+ *     structural rewrites: fused QKV projections whose single operator also
+ *     normalizes Q and K and applies the rotary embeddings, and fused
+ *     GELU/MLP kernels -- here svdq_gemm_w4a4_qkv and svdq_gemm_w4a4_gelu,
+ *     the same 4-bit product with those steps in its epilogue.
  *
  *   Y = Q4(X_hat) Q4(R) s_T + (X L1s) L2 + b,    X_hat = X diag(inv_lambda)
  *
