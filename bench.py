@@ -351,18 +351,20 @@ def run_gpu(args, world, rank, local):
     if args.awq_blocks > 0:
         awq = run_awq(args, lib, dev, stream, world)
 
-    # the tensor cores' own NVFP4 rate on this device: back-to-back
-    # M128 N256 K64 block-scaled MMAs on every SM (no memory traffic)
+    # the tensor cores' own NVFP4 rate on this device, at the GEMM's shape:
+    # back-to-back CTA-pair M256 N256 K64 block-scaled MMAs on every SM pair
+    # (no memory traffic)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ctas = 2 * (sms // 2)
     iters = 8192
     for _ in range(2):
-        lib.bench_mma_rate(0, 256, iters, sms, dev_status=status, stream=stream)
+        lib.bench_mma_rate(3, 256, iters, ctas, dev_status=status, stream=stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    lib.bench_mma_rate(0, 256, iters, sms, dev_status=status, stream=stream)
+    lib.bench_mma_rate(3, 256, iters, ctas, dev_status=status, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    mma_tflops = 2.0 * 128 * 256 * 64 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    mma_tflops = 2.0 * 128 * 256 * 64 * iters * ctas / (e0.elapsed_time(e1) * 1e-3) / 1e12
 
     pk = peaks()
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16

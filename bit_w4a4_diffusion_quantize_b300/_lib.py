@@ -53,6 +53,7 @@ _SIGS = {
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
+    "svdq_test_set_hooks": (_i32, [_i32, _i32]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -323,3 +324,11 @@ def bench_mma_rate(mode: int, n: int, iters: int, ctas: int, dev_status=None, st
     CUDA events on `stream`."""
     _check(_lib.svdq_bench_mma_rate(int(mode), int(n), int(iters), int(ctas), _dptr(dev_status),
                                     _stream_ptr(stream)), "svdq_bench_mma_rate")
+
+
+def test_set_hooks(fake_compute_capability: int = 0, gemm_stall: int = 0):
+    """Test hooks of the library (include/svdq_test.h): a compute capability to
+    report instead of the device's (10 * major + minor, 0 = off) and a GEMM
+    loader that issues nothing (1), so that its bounded waits run out."""
+    _check(_lib.svdq_test_set_hooks(int(fake_compute_capability), int(gemm_stall)),
+           "svdq_test_set_hooks")

@@ -54,7 +54,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "svdq.h"),
-                                                       os.path.join(INCLUDE, "svdq_bench.h")]
+                                                       os.path.join(INCLUDE, "svdq_bench.h"),
+                                                       os.path.join(INCLUDE, "svdq_test.h")]
     objs = []
     for src in CUDA_SOURCES:
         s = os.path.join(CSRC, src)

@@ -10,12 +10,11 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/svdq.h"
+#include "../../include/svdq_test.h"
 #include "launch.h"
 
 namespace {
@@ -31,19 +30,22 @@ DeviceInfo g_dev[kMaxDevices];
 // Compute capability required by the sm_103a kernels.
 constexpr int kMajor = 10, kMinor = 3;
 
+// Test hooks, set only through svdq_test_set_hooks (include/svdq_test.h):
+// a compute capability to report instead of the device's (10 * major +
+// minor; 0 = off), and a GEMM whose loader issues nothing.
+std::atomic<int> g_fake_cc{0};
+std::atomic<int> g_gemm_stall{0};
+
 svdq_status current_device(int* dev_out, int* num_sms) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return SVDQ_ERR_CUDA;
   }
-  // test hook: pretend the device has another compute capability ("MAJOR.MINOR")
-  const char* fake = std::getenv("SVDQ_FAKE_COMPUTE_CAPABILITY");
-  if (fake && *fake) {
-    int ma = 0, mi = 0;
-    if (std::sscanf(fake, "%d.%d", &ma, &mi) >= 1 && (ma != kMajor || mi != kMinor))
-      return SVDQ_ERR_UNSUPPORTED_ARCH;
-  }
+  // test hook (svdq_test_set_hooks): pretend the device has another compute
+  // capability
+  const int fake = g_fake_cc.load(std::memory_order_relaxed);
+  if (fake != 0 && fake != 10 * kMajor + kMinor) return SVDQ_ERR_UNSUPPORTED_ARCH;
   DeviceInfo& d = g_dev[dev];
   int st = d.state.load(std::memory_order_acquire);
   if (st == 0) {
@@ -183,7 +185,7 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
   if (is_qkv && N % 768 != 0) return SVDQ_ERR_SHAPE;  // Q, K, V: whole pairs of 128-wide heads
   if (!rank_ok(rank)) return SVDQ_ERR_RANK;
-  if (is_qkv && !(std::isfinite(qe.eps) && qe.eps >= 0.0f)) return SVDQ_ERR_VALUE;
+  if (is_qkv && !(std::isfinite(qe.eps) && qe.eps > 0.0f)) return SVDQ_ERR_VALUE;
   {
     // a finite power of two in [2^-100, 2^100]
     int ex = 0;
@@ -211,12 +213,14 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
   if (!encode_codes(&maps.a_codes, a_codes, M, K, 128) ||
       !encode_codes(&maps.w_codes, w_codes, N, K, block_n / 2) ||
       !encode_rank_rows(&maps.lora, lora_act, M, rank, 128) ||
-      !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n))
+      !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n / 2) ||
+      !encode_2d(&maps.y, CU_TENSOR_MAP_DATA_TYPE_UINT16, Y, (uint64_t)N, (uint64_t)M,
+                 (uint64_t)N * 2, (uint32_t)(block_n / 4), 32u,
+                 block_n == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
     return SVDQ_ERR_CUDA;
-  // test hook: SVDQ_TEST_GEMM_STALL=1 makes the kernel's loader issue nothing
-  // so that its pipeline wait times out after 100 ms (status SVDQ_DEV_TIMEOUT)
-  const char* stall = std::getenv("SVDQ_TEST_GEMM_STALL");
-  const int test_stall = (stall && stall[0] == '1') ? 1 : 0;
+  // test hook: the kernel's loader issues nothing, so that its pipeline waits
+  // time out after 100 ms (status SVDQ_DEV_TIMEOUT)
+  const int test_stall = g_gemm_stall.load(std::memory_order_relaxed) ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
                                          bias, Y, M, N, K, rank, epi, qe, dev_status,
                                          test_stall, sms, static_cast<cudaStream_t>(stream));
@@ -280,3 +284,10 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
 }
 
 }  // extern "C"
+
+extern "C" svdq_status svdq_test_set_hooks(int fake_compute_capability, int gemm_stall) {
+  if (fake_compute_capability < 0 || (gemm_stall != 0 && gemm_stall != 1)) return SVDQ_ERR_VALUE;
+  g_fake_cc.store(fake_compute_capability, std::memory_order_relaxed);
+  g_gemm_stall.store(gemm_stall, std::memory_order_relaxed);
+  return SVDQ_OK;
+}

@@ -188,7 +188,6 @@ SVDQ_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
     }
   }
 }
-
 SVDQ_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -217,24 +216,6 @@ SVDQ_DEVINL void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uin
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-// The same loads, delivered to the same shared-memory offset (and completing
-// on the mbarrier at the same offset) in every CTA of the cluster in `mask`.
-SVDQ_DEVINL void tma_load_2d_mc(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y,
-                                uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-SVDQ_DEVINL void bulk_load_mc(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
-                              uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
 }
 // ---------------------------------------------------------------- dependent launch
@@ -334,13 +315,114 @@ SVDQ_DEVINL void tc_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-// the same commit, arriving once on the mbarrier at this offset in every CTA
-// of the cluster in `mask`
-SVDQ_DEVINL void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+// ---- CTA-pair forms (cta_group::2): one MMA spans the TMEM lanes of two SMs.
+// Allocation and release are collective: one warp of each CTA of the pair
+// executes them, with the same column count, while both CTAs are resident.
+SVDQ_DEVINL void tmem_alloc_pair(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+SVDQ_DEVINL void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// shared::cluster address of the object at CTA-local shared address `saddr`
+// in CTA `rank` of the cluster
+SVDQ_DEVINL uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// one arrive on an mbarrier given by its shared::cluster address (this CTA's
+// or the peer's).  Default semantics (release, CTA scope) as for a local
+// arrive: what the pair signals this way is the completion of work that is
+// already finished where it happened (TMEM stores waited for with
+// tcgen05.wait::st, TMA copies whose barrier phase completed, TMEM loads
+// waited for with tcgen05.wait::ld).  A cluster-scope release or acquire
+// costs about half a microsecond per use on this part.
+SVDQ_DEVINL void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// completion of every prior tcgen05 async op of this thread (pair MMAs) as one
+// arrive on the mbarrier at shared::cluster address `cluster_addr`
+SVDQ_DEVINL void tc_commit_pair(uint32_t cluster_addr) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          cluster_addr)
+      : "memory");
+}
+// pair NVFP4 MMA (issued by one thread of the even CTA): D rows 0-127 in the
+// even CTA's TMEM, 128-255 in the odd CTA's; each CTA supplies its own 128 A
+// rows and one half of the B rows from its shared memory at the same offsets;
+// scale addresses name the same TMEM columns in both CTAs
+SVDQ_DEVINL void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                  uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.u32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+SVDQ_DEVINL void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Warp-wide forms of the pair MMA and commit: every lane of a converged warp
+// executes them with the same (warp-uniform) operands and one lane, picked by
+// elect.sync, issues the instruction.  Kept warp-uniform, the operands stay in
+// uniform registers: the issue of a tcgen05 instruction from one divergent
+// lane costs about 75 cycles of operand moves, more than the tensor cores
+// need to run an NVFP4 MMA when back-to-back issue is what keeps them busy.
+SVDQ_DEVINL void tc_mma_nvf4_pair_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\n"
+      "setp.ne.u32 p, %6, 0;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+SVDQ_DEVINL void tc_mma_bf16_pair_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p, e;\n"
+      "setp.ne.u32 p, %4, 0;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// the same commit to two barriers (one elected lane issues both)
+SVDQ_DEVINL void tc_commit_pair_warp2(uint32_t cluster_addr0, uint32_t cluster_addr1) {
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%1];\n}" ::"r"(
+          cluster_addr0),
+      "r"(cluster_addr1)
+      : "memory");
+}
+SVDQ_DEVINL void tc_commit_pair_warp(uint32_t cluster_addr) {
+  asm volatile(
+      "{\n.reg .pred e;\n"
+      "elect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(
+          cluster_addr)
       : "memory");
 }
 // block-scaled NVFP4 MMA: D(tmem) (+)= A(smem) x B(smem), scales in TMEM

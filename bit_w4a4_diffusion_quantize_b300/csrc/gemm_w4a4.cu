@@ -17,55 +17,67 @@
 //      article, structural rewrites: one fused operator for the QKV
 //      projection, the Q/K normalization and the rotary embeddings)
 //
-// Persistent kernel in clusters of two CTAs (one CTA per SM).  A cluster walks
-// pairs of 128 x BN output tiles that share their columns (BN = 256, or 128
-// when N is not a multiple of 256): CTA rank r of the pair computes m tile
-// 2p + r.  The W operand of a k tile (BN code rows and their scales) is the
-// same for both CTAs, so each CTA loads half of it and multicasts it into both
-// CTAs' shared memory: per SM a k tile then moves 2/3 of the bytes of an
-// unpaired CTA.  A ring slot may be refilled only when both CTAs' MMAs are
-// done with it: each CTA's MMA commit arrives on the `empty` barrier of both.
+// Persistent kernel in clusters of two CTAs (one CTA per SM) that compute
+// together with the tensor cores' CTA-pair MMAs (tcgen05 cta_group::2).  A
+// pair walks 256 x BN output tiles (BN = 256, or 128 when N is not a multiple
+// of 256), N fastest.  One M = 256 MMA covers the pair's tile: CTA rank c
+// holds output rows 128c .. 128c + 127 in its TMEM, its own 128 A rows and
+// one half of the tile's W rows (BN/2 of them) in its shared memory; the
+// tensor cores of the two SMs exchange the W halves themselves.  So every
+// byte a CTA loads is its own: per SM a k tile moves 38 KB (A 16 KB, W half
+// 16 KB, block scales 6 KB) for the same 16.8 MFLOP that a lone 128 x 256
+// tile would need 54 KB for.
 //
-// The ring (4 slots of 54 KB at BN = 256) carries, per output tile, its k
-// tiles -- A code tile and scale chunk (own), half of the W code rows and
-// scale chunks (multicast); 128-byte rows, 128B swizzle; the scale layout is
-// already the tensor core's, so scales move as plain bulk copies -- and then
-// one slot with the tile's rank-r operands (lora rows in the A area, L2s rows
-// in the B area, K-major, swizzled TMA boxes) plus its bias slice (into a
-// separate double buffer that the epilogue releases).
+// Each CTA's ring (5 slots of 38 KB at BN = 256) carries, per output tile,
+// its k tiles -- A code tile and its scale chunk, the CTA's half of the W code
+// rows, and the scale chunks of all BN W rows (both halves: the MMA of each
+// SM needs every column's scales in its own TMEM); 128-byte rows, 128B
+// swizzle; the scale layout is already the tensor core's, so scales move as
+// plain bulk copies -- and then one slot with the tile's rank-r operands
+// (lora rows in the A area, the CTA's half of the L2s rows in the B area,
+// K-major, swizzled TMA boxes) plus the tile's bias slice (into a separate
+// double buffer that the epilogue releases).
 //
 // Warp roles (22 warps per CTA; a warp reaches TMEM lanes 32 * (warp % 4)):
-//   warp 0     one lane: the producer of the ring, running ahead across tiles;
-//   warp 1     allocates TMEM; one lane issues the block-scaled MMAs of each
-//              k tile, then the rank-r MMAs into the same accumulator;
-//              tcgen05.commit frees ring slots (in both CTAs) and finally
-//              signals `acc_full`;
+//   warp 0     one lane: the producer of this CTA's ring, running ahead
+//              across tiles;
+//   warp 1     allocates TMEM (collectively with the peer); in the even CTA
+//              one lane issues the pair MMAs of each k tile, then the rank-r
+//              MMAs into the same accumulator; tcgen05.commit frees the ring
+//              slots of both CTAs and finally signals `acc_full` in both;
 //   warps 2-5  scale warps, one per TMEM lane quarter: for each k tile they
-//              move the block scales from shared memory into TMEM with
-//              tcgen05.st (registers -> TMEM), keeping that traffic off the
-//              MMA issue path, and signal `sf_full`;
+//              move the block scales from shared memory into this CTA's TMEM
+//              with tcgen05.st (registers -> TMEM), keeping that traffic off
+//              the MMA issue path, and report to the even CTA's `sf_full`
+//              (that report also tells the issuer that this CTA's slot has
+//              landed);
 //   warps 6-21 the epilogue, four per TMEM lane quarter (one output row per
 //              lane, BN/4 columns each): one tcgen05.ld of their columns, and
-//              `acc_empty` is released at once -- the single accumulator is
-//              held only for that load; then y = s_T * acc + bias rounded to
-//              bf16 pairs (QKV: the two warps holding the halves of a head
-//              swap their rows' partial sums of squares through shared memory
-//              behind a two-warp barrier, then normalize and rotate), and an
-//              8 x 8 (4 x 4 at BN = 128) transpose of
-//              16-byte chunks inside groups of lanes (warp shuffles) turns
-//              "one row per lane" into "8 lanes per row": each store
-//              instruction writes 4 whole 128-byte row segments.
+//              the even CTA's `acc_empty` is told at once -- the single
+//              accumulator is held only for that load; then y = s_T * acc +
+//              bias rounded to bf16 pairs (QKV: the two warps holding the
+//              halves of a head swap their rows' partial sums of squares
+//              through shared memory behind a two-warp barrier, then
+//              normalize and rotate), and an 8 x 8 (4 x 4 at BN = 128)
+//              transpose of 16-byte chunks inside groups of lanes (warp
+//              shuffles) turns "one row per lane" into "8 lanes per row": each
+//              store instruction writes 4 whole 128-byte row segments.
 //
 // Block scales in TMEM.  Per 64-wide K step, the 128 x 4 scale chunk of A
 // (512 bytes, row r at byte (r%32)*16 + (r/32)*4) occupies 4 columns: every
 // lane quarter holds, in lane l, column j, the 4 scales of row l + 32j (the
 // layout of tcgen05.cp.32x128b.warpx4).  A scale warp loads chunk row l (16
 // bytes) and stores it with one tcgen05.st.32x32b.x4.  B's BN rows take BN/32
-// columns the same way.
+// columns the same way, in each CTA of the pair.
+//
+// Cross-CTA signals are plain mbarrier arrivals on shared::cluster addresses
+// (mapa) and tcgen05.commit to each CTA's barrier in turn; no data moves
+// between the two shared memories except through the pair MMA.
 //
 // Every wait is bounded: on timeout the kernel reports SVDQ_DEV_TIMEOUT,
-// stops issuing work, lets the copies and MMAs in flight land, frees TMEM and
-// returns.
+// tells the peer CTA to stop too, stops issuing work, lets the copies and MMAs
+// in flight land, frees TMEM and returns.
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -76,16 +88,16 @@ namespace svdq {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BM = 128;              // output rows per CTA (TMEM lanes); a pair covers 256
 constexpr int BK_BYTES = 128;        // one k tile: 256 fp4 values per row
 constexpr int KB_PER_TILE = 4;       // 64-wide MMA steps per k tile
-constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
 constexpr int NUM_THREADS = 22 * 32;
 constexpr int SF_WARP0 = 2;   // warps 2..5
 constexpr int EPI_WARP0 = 6;  // warps 6..21
 constexpr int EPI_WARPS = 16;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BUDGET = 224 * 1024;
+constexpr int kMaxDevices = 64;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
@@ -96,14 +108,15 @@ constexpr int kHeadDim = 128;  // QKV epilogue: channels of one head
 
 template <int BN, int RANK, int EPI>
 struct Cfg {
+  static constexpr int BH = BN / 2;  // W rows held by one CTA of the pair
   static constexpr int A_BYTES = BM * BK_BYTES;
-  static constexpr int B_BYTES = BN * BK_BYTES;
+  static constexpr int B_BYTES = BH * BK_BYTES;
   static constexpr int SFA_BYTES = KB_PER_TILE * 512;
-  static constexpr int SFB_BYTES = KB_PER_TILE * 512 * (BN / 128);
+  static constexpr int SFB_BYTES = KB_PER_TILE * 512 * (BN / 128);  // all BN rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int LROW = RANK * 2;  // bytes of one rank-r row (bf16)
   static constexpr int LA_BYTES = BM * LROW;
-  static constexpr int LB_BYTES = BN * LROW;
+  static constexpr int LB_BYTES = BH * LROW;
   static_assert(LA_BYTES <= A_BYTES && LB_BYTES <= B_BYTES, "rank-r operands fit a ring slot");
   static constexpr int BIAS_BYTES = BN * 2;
   static constexpr int MISC_BYTES = 512;
@@ -111,50 +124,68 @@ struct Cfg {
   // (two buffers), and one barrier per warp pair
   static constexpr int XSUM_BYTES = EPI == kEpiQkv ? 2 * 16 * 32 * 4 : 0;
   static constexpr int PAIR_BARS = EPI == kEpiQkv ? 8 : 0;
-  static constexpr int FIXED_BYTES = 2 * BIAS_BYTES + XSUM_BYTES + MISC_BYTES;
-  static constexpr int STAGES = cmin(6, (SMEM_BUDGET - 1024 - FIXED_BYTES) / STAGE_BYTES);
-  static constexpr int OFF_A = 0;  // slot areas 1024-aligned (swizzle atoms)
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_BIAS = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_XSUM = OFF_BIAS + 2 * BIAS_BYTES;
-  static constexpr int OFF_BAR = OFF_XSUM + XSUM_BYTES;
-  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full, acc_empty,
-  // pair[PAIR_BARS]
-  static constexpr int NUM_BARS = 3 * STAGES + 4 + PAIR_BARS;
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + base alignment slack
+  static constexpr int EPI_COLS = BN / 4;     // columns per epilogue warp
+  static constexpr int EPI_CH = EPI_COLS / 8;  // 16-byte output chunks per row and warp
+  // plain and GELU epilogues: each warp stages its 32 x EPI_COLS bf16 block in
+  // shared memory (the swizzled layout of the output tensor map) and stores it
+  // with one TMA store; QKV stores from registers after a lane transpose
+  static constexpr bool TMA_OUT = EPI != kEpiQkv;
+  static constexpr int OUT_ROW_BYTES = EPI_COLS * 2;                 // 128 or 64
+  static constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
+  static constexpr int OUT_BYTES = TMA_OUT ? EPI_WARPS * OUT_WARP_BYTES : 0;
+  static constexpr int FIXED_BYTES = OUT_BYTES + 2 * BIAS_BYTES + XSUM_BYTES + MISC_BYTES;
   // TMEM columns: accumulator [0, BN), then per stage the scales of A and B
   static constexpr int SF_COLS_A = 4 * KB_PER_TILE;
   static constexpr int SF_COLS_B = 4 * KB_PER_TILE * (BN / 128);
   static constexpr int SF_STAGE_COLS = SF_COLS_A + SF_COLS_B;
   static constexpr int SF_BASE = BN;
+  static constexpr int STAGES =
+      cmin(cmin(6, (SMEM_BUDGET - 1024 - FIXED_BYTES) / STAGE_BYTES),
+           ((int)TMEM_COLS - SF_BASE) / SF_STAGE_COLS);
+  static constexpr int OFF_A = 0;  // slot areas 1024-aligned (swizzle atoms)
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 1024-aligned
+  static constexpr int OFF_BIAS = OFF_OUT + OUT_BYTES;
+  static constexpr int OFF_XSUM = OFF_BIAS + 2 * BIAS_BYTES;
+  static constexpr int OFF_BAR = OFF_XSUM + XSUM_BYTES;
+  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full,
+  // acc_empty, mma_done, pair[PAIR_BARS]
+  static constexpr int NUM_BARS = 3 * STAGES + 5 + PAIR_BARS;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + base alignment slack
   static_assert(STAGES >= 2, "pipeline depth");
   static_assert(SF_BASE + STAGES * SF_STAGE_COLS <= (int)TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(B_BYTES % 1024 == 0, "W half tiles keep the 1024-byte swizzle atoms aligned");
   static constexpr SmemLayout LSW =
       LROW == 128 ? kSwizzle128B : (LROW == 64 ? kSwizzle64B : kSwizzle32B);
-  // instruction descriptors (kind::mxf4nvf4: E2M1 x E2M1, UE4M3 scales, K-major,
-  // M = 128, N = BN; kind::f16: bf16 x bf16 -> f32)
+  // instruction descriptors of the pair MMAs (kind::mxf4nvf4: E2M1 x E2M1,
+  // UE4M3 scales, K-major, M = 256 over the pair, N = BN; kind::f16: bf16 x
+  // bf16 -> f32)
   static constexpr uint32_t IDESC_NVF4 = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                                         ((uint32_t)(BM >> 4) << 24);
+                                         ((uint32_t)((2 * BM) >> 4) << 24);
   static constexpr uint32_t IDESC_BF16 = (1u << 4) | (1u << 7) | (1u << 10) |
-                                         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-  static constexpr int EPI_COLS = BN / 4;  // columns per epilogue warp
-  static constexpr int EPI_CH = EPI_COLS / 8;  // 16-byte output chunks per row and warp
+                                         ((uint32_t)(BN >> 3) << 17) |
+                                         ((uint32_t)((2 * BM) >> 4) << 24);
+  static_assert(OFF_OUT % 1024 == 0, "staging areas keep the swizzle atoms aligned");
 };
 
 #ifdef SVDQ_GEMM_TRACE
 // timeline instrumentation, compiled only into instrumented builds: the first
 // 8 CTAs stamp %globaltimer at fixed slots (1024 per CTA)
 __device__ unsigned long long* g_gemm_trace = nullptr;
+#define SVDQ_TR_SETUP unsigned long long* const trace_ = g_gemm_trace
 #define SVDQ_TR(slot, lim, idx)                                                   \
   do {                                                                            \
-    if (g_gemm_trace && blockIdx.x < 8 && (idx) < (lim))                          \
-      g_gemm_trace[blockIdx.x * 1024 + (slot) + (idx)] = globaltimer_ns();        \
+    if (trace_ && blockIdx.x < 8 && (idx) < (lim))                                \
+      trace_[blockIdx.x * 1024 + (slot) + (idx)] = globaltimer_ns();              \
   } while (0)
 #else
+#define SVDQ_TR_SETUP \
+  do {                \
+  } while (0)
 #define SVDQ_TR(slot, lim, idx) \
   do {                          \
   } while (0)
@@ -277,53 +308,68 @@ template <int BN, int RANK, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_w4a4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_lora,
-                const __grid_constant__ CUtensorMap tm_l2s, const uint8_t* __restrict__ a_scales,
+                const __grid_constant__ CUtensorMap tm_l2s,
+                const __grid_constant__ CUtensorMap tm_y, const uint8_t* __restrict__ a_scales,
                 const uint8_t* __restrict__ w_scales, float s_T,
                 const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
                 const QkvEpilogue qe, int* dev_status, int test_stall, uint64_t wait_ns) {
   static_assert(EPI != kEpiQkv || BN == 2 * kHeadDim, "QKV epilogue: two heads per tile");
   using C = Cfg<BN, RANK, EPI>;
   constexpr int STAGES = C::STAGES;
+  SVDQ_TR_SETUP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
-  uint64_t* sf_full = empty + STAGES;
+  uint64_t* sf_full = empty + STAGES;       // used in the even CTA
   uint64_t* bias_empty = sf_full + STAGES;  // [2]
   uint64_t* acc_full = bias_empty + 2;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* pair_bar = acc_empty + 1;  // [PAIR_BARS]
+  uint64_t* acc_empty = acc_full + 1;       // used in the even CTA
+  uint64_t* mma_done = acc_empty + 1;       // used in the even CTA
+  uint64_t* pair_bar = mma_done + 1;        // [PAIR_BARS]
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
   volatile uint32_t* abort_flag = &misc[1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = (int)cluster_ctarank();  // 0 or 1 within the pair
+  const uint32_t crank = cluster_ctarank();  // 0 (issues the pair MMAs) or 1
   const int kb_total = K >> 6;               // 64-wide steps
   const int k_tiles = (kb_total + KB_PER_TILE - 1) / KB_PER_TILE;
   const int n_tiles = N / BN;
   const int m_tiles = (M + BM - 1) / BM;
-  const int num_ptiles = ((m_tiles + 1) / 2) * n_tiles;  // tile pairs
+  const int num_ptiles = ((m_tiles + 1) / 2) * n_tiles;  // 256-row pair tiles
   const int pair = (int)blockIdx.x >> 1, n_pairs = (int)gridDim.x >> 1;
   const int my_tiles = pair < num_ptiles ? (num_ptiles - 1 - pair) / n_pairs + 1 : 0;
   // tile j of this CTA: m tile 2 * (pt / n_tiles) + crank (may lie past M when
   // m_tiles is odd: it is computed on zero-filled rows and not stored)
   auto tile_mn = [&](int j, int& m_tile, int& n_tile) {
     const int pt = pair + j * n_pairs;
-    m_tile = 2 * (pt / n_tiles) + crank;
+    m_tile = 2 * (pt / n_tiles) + (int)crank;
     n_tile = pt % n_tiles;
+  };
+  // the even CTA's copy of a barrier, as a shared::cluster address
+  auto at_even = [](uint64_t* bar) { return cluster_map(smem_u32(bar), 0u); };
+  // stop this CTA and tell the peer to stop too (its waits would otherwise
+  // run into their own bounds one after another)
+  auto abort_pair = [&]() {
+    *abort_flag = 1;
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(
+                     cluster_map(smem_u32(&misc[1]), crank ^ 1u)),
+                 "r"(1u)
+                 : "memory");
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // the MMA commits of both CTAs of the pair
-      mbar_init(&sf_full[s], 128);
+      mbar_init(&empty[s], 1);     // the even CTA's MMA commit
+      mbar_init(&sf_full[s], 8);   // the 4 scale warps of each CTA of the pair
     }
     mbar_init(&bias_empty[0], EPI_WARPS);
     mbar_init(&bias_empty[1], EPI_WARPS);
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, EPI_WARPS * 32);
+    mbar_init(acc_empty, 2 * EPI_WARPS);  // the epilogue warps of both CTAs
+    mbar_init(mma_done, 1);
     for (int b = 0; b < C::PAIR_BARS; ++b) mbar_init(&pair_bar[b], 2);
     misc[1] = 0;
     fence_mbar_init();
@@ -331,10 +377,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tm_b);
     prefetch_tmap(&tm_lora);
     prefetch_tmap(&tm_l2s);
+    if (C::TMA_OUT) prefetch_tmap(&tm_y);
   }
-  if (warp == 1) tmem_alloc(&misc[0], TMEM_COLS);
+  // both CTAs resident and their barriers initialised before the collective
+  // TMEM allocation and before any arrival from the peer
+  cluster_sync();
+  if (warp == 1) tmem_alloc_pair(&misc[0], TMEM_COLS);
   tc_fence_before();
-  cluster_sync();  // the peer's barriers exist before anything is multicast to them
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   grid_dep_launch();
@@ -349,51 +399,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tile_mn(j, m_tile, n_tile);
         const bool m_valid = m_tile < m_tiles;
         const int m0 = m_tile * BM, n0 = n_tile * BN;
+        const int nh = n0 + (int)crank * C::BH;  // this CTA's half of the W rows
         for (int kt = 0; kt <= k_tiles; ++kt) {  // k tiles, then the rank-r slot
           const int s = issued % STAGES;
           const uint32_t ph = (uint32_t)(issued / STAGES) & 1u;
           if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, dev_status, wait_ns)) {
-            *abort_flag = 1;
+            abort_pair();
             break;
           }
+          SVDQ_TR(832, 128, issued);
           uint8_t* sa = smem + C::OFF_A + s * C::A_BYTES;
           uint8_t* sb = smem + C::OFF_B + s * C::B_BYTES;
           if (kt == k_tiles) {
-            // rank-r operands of tile j (own loads) and its bias slice
+            // rank-r operands of tile j (own rows, own half of L2s) and its
+            // bias slice (all BN columns: this CTA stores every column)
             if (bias && !mbar_wait(&bias_empty[j & 1], (uint32_t)((j >> 1) & 1) ^ 1u,
                                    dev_status, wait_ns)) {
-              *abort_flag = 1;
+              abort_pair();
               break;
             }
             mbar_arrive_expect_tx(&full[s], (uint32_t)(C::LA_BYTES + C::LB_BYTES +
                                                        (bias ? C::BIAS_BYTES : 0)));
             tma_load_2d(sa, &tm_lora, &full[s], 0, m0);
-            tma_load_2d(sb, &tm_l2s, &full[s], 0, n0);
+            tma_load_2d(sb, &tm_l2s, &full[s], 0, nh);
             if (bias)
               bulk_load(smem + C::OFF_BIAS + (j & 1) * C::BIAS_BYTES, bias + n0,
                         (uint32_t)C::BIAS_BYTES, &full[s]);
             SVDQ_TR(424, 8, j);
           } else {
             const int nkb = min(KB_PER_TILE, kb_total - kt * KB_PER_TILE);
-            // this CTA's stage: its A tile (+ scales, rows inside M), all BN W
-            // rows and their scales (half from each CTA of the pair)
+            // this CTA's A tile (+ its scales, rows inside M), its half of the
+            // W rows, and the scales of all BN W rows
             const uint32_t bytes = (uint32_t)(C::A_BYTES + C::B_BYTES +
                                               nkb * 512 * ((m_valid ? 1 : 0) + BN / 128));
             mbar_arrive_expect_tx(&full[s], bytes);
             tma_load_2d(sa, &tm_a, &full[s], kt * BK_BYTES, m0);
-            tma_load_2d_mc(sb + crank * (C::B_BYTES / 2), &tm_b, &full[s], kt * BK_BYTES,
-                           n0 + crank * (BN / 2), kPairMask);
+            tma_load_2d(sb, &tm_b, &full[s], kt * BK_BYTES, nh);
             if (m_valid)
               bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
                         a_scales + ((size_t)m_tile * kb_total + (size_t)kt * KB_PER_TILE) * 512,
                         (uint32_t)nkb * 512u, &full[s]);
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)
-              if ((h & 1) == crank)
-                bulk_load_mc(smem + C::OFF_SFB + s * C::SFB_BYTES + h * KB_PER_TILE * 512,
-                             w_scales + ((size_t)(n0 / 128 + h) * kb_total +
-                                         (size_t)kt * KB_PER_TILE) * 512,
-                             (uint32_t)nkb * 512u, &full[s], kPairMask);
+              bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + h * KB_PER_TILE * 512,
+                        w_scales + ((size_t)(n0 / 128 + h) * kb_total +
+                                    (size_t)kt * KB_PER_TILE) * 512,
+                        (uint32_t)nkb * 512u, &full[s]);
             SVDQ_TR(0, 128, issued);
           }
           ++issued;
@@ -401,73 +452,135 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int it = 0;  // ring position
-      for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
-        if (!mbar_wait(acc_empty, (uint32_t)(j & 1) ^ 1u, dev_status, wait_ns)) {
-          *abort_flag = 1;
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    // The tensor cores queue only about one MMA ahead, so this thread keeps
+    // the work between two MMAs short: descriptors are formed by adding to
+    // per-ring constants, the ring position advances without division, and
+    // the wait for the next ring position runs while the current position's
+    // last MMA is still queued.
+    if (crank == 0) {  // the whole warp, converged; one elected lane issues
+      const uint64_t a_desc0 = smem_desc(smem_u32(smem + C::OFF_A), 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::OFF_B), 16, 1024, kSwizzle128B);
+      const uint32_t empty_c0 = cluster_map(smem_u32(empty), 0u);
+      const uint32_t empty_c1 = cluster_map(smem_u32(empty), 1u);
+      const bool tail_half = (kb_total % KB_PER_TILE) != 0;  // last k tile has 2 MMA steps
+      int s = 0;
+      uint32_t ph = 0;  // ring position: slot and phase parity
+      // Position (s, ph) is ready when the scale warps of both CTAs have seen
+      // their slot land and put its scales in their TMEM (sf_full: the scale
+      // warps waited on this CTA's `full` first, so it orders the TMA data too).
+      auto ready = [&](int s_, uint32_t ph_) -> bool {
+        const bool ok = mbar_wait(&sf_full[s_], ph_, dev_status, wait_ns);
+        tc_fence_after();
+        return __all_sync(0xFFFFFFFFu, ok);
+      };
+      // frees slot s in both CTAs once the MMAs issued so far have read it
+      auto release_slot = [&](int s_) {
+        tc_commit_pair_warp2(empty_c0 + 8u * (uint32_t)s_, empty_c1 + 8u * (uint32_t)s_);
+      };
+      for (int j = 0; j < my_tiles && !__any_sync(0xFFFFFFFFu, *abort_flag != 0); ++j) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_empty, (uint32_t)(j & 1) ^ 1u, dev_status,
+                                                 wait_ns))) {
+          abort_pair();
           break;
         }
         tc_fence_after();
         SVDQ_TR(384, 8, j);
-        bool ok = true;
-        for (int kt = 0; kt < k_tiles; ++kt, ++it) {
-          const int s = it % STAGES;
-          // sf_full: the scale warps saw the stage land and put its scales in
-          // TMEM; full (already complete then) orders the TMA data for the MMAs
-          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-          if (*abort_flag || !mbar_wait(&sf_full[s], ph, dev_status, wait_ns) ||
-              !mbar_wait(&full[s], ph, dev_status, wait_ns)) {
-            ok = false;
-            break;
+        bool ok = ready(s, ph);
+        int prev = -1;  // slot whose release waits until the next MMA is queued
+        uint64_t ad = a_desc0 + (uint64_t)((s * C::A_BYTES) >> 4);
+        uint64_t bd = b_desc0 + (uint64_t)((s * C::B_BYTES) >> 4);
+        uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
+        for (int kt = 0; kt < k_tiles && ok; ++kt) {
+          SVDQ_TR(128, 128, kt + j * (k_tiles + 1));
+          const uint32_t sfb = sfa + (uint32_t)C::SF_COLS_A;
+          // MMA step kb: K offset 32 bytes per step (2 in the descriptor's
+          // 16-byte address units), scale columns 4 (A) and 4 BN/128 (B) per step
+          auto mma = [&](int kb, uint32_t acc) {
+            tc_mma_nvf4_pair_warp(tmem, ad + (uint64_t)(2 * kb), bd + (uint64_t)(2 * kb),
+                                  C::IDESC_NVF4, sfa + 4u * kb, sfb + 4u * (BN / 128) * kb, acc);
+          };
+          int sn = s + 1;
+          uint32_t phn = ph;
+          if (sn == STAGES) {
+            sn = 0;
+            phn ^= 1u;
           }
-          tc_fence_after();
-          SVDQ_TR(128, 128, it);
-          const int nkb = min(KB_PER_TILE, kb_total - kt * KB_PER_TILE);
-          const uint32_t a_base = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-          const uint32_t b_base = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-          const uint32_t sf_col = (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
-          for (int kb = 0; kb < nkb; ++kb)
-            tc_mma_nvf4(tmem, smem_desc(a_base + kb * 32, 16, 1024, kSwizzle128B),
-                        smem_desc(b_base + kb * 32, 16, 1024, kSwizzle128B), C::IDESC_NVF4,
-                        tmem + sf_col + kb * 4,
-                        tmem + sf_col + C::SF_COLS_A + kb * 4 * (BN / 128),
-                        (kt | kb) != 0 ? 1u : 0u);
-          tc_commit_mc(&empty[s], kPairMask);  // frees the slot in both CTAs
-          SVDQ_TR(256, 128, it);
+          // the slow steps (commits, barrier waits) each go where an MMA is
+          // already queued: release of the previous slot after this slot's
+          // first MMA, the wait for the next position after its second
+          mma(0, kt != 0 ? 1u : 0u);
+          if (prev >= 0) release_slot(prev);
+          if (tail_half && kt + 1 == k_tiles) {
+            ok = ready(sn, phn);
+            mma(1, 1u);
+          } else {
+            mma(1, 1u);
+            ok = ready(sn, phn);
+            mma(2, 1u);
+            mma(3, 1u);
+          }
+          SVDQ_TR(256, 128, kt + j * (k_tiles + 1));
+          prev = s;
+          s = sn;
+          ph = phn;
+          if (sn == 0) {
+            ad = a_desc0;
+            bd = b_desc0;
+            sfa = tmem + (uint32_t)C::SF_BASE;
+          } else {
+            ad += (uint64_t)(C::A_BYTES >> 4);
+            bd += (uint64_t)(C::B_BYTES >> 4);
+            sfa += (uint32_t)C::SF_STAGE_COLS;
+          }
         }
         if (ok) {
-          // the rank-r slot (the scale warps mark it in sf_full too, so that
-          // every slot's sf_full completes once per use of the slot)
-          const int s = it % STAGES;
-          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-          if (!*abort_flag && mbar_wait(&sf_full[s], ph, dev_status, wait_ns) &&
-              mbar_wait(&full[s], ph, dev_status, wait_ns)) {
-            tc_fence_after();
-            SVDQ_TR(392, 8, j);
-            const uint32_t la = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-            const uint32_t lbp = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+          // the rank-r slot (the scale warps report it in sf_full too, so that
+          // every slot's sf_full completes once per use of the slot); its
+          // readiness was awaited during the last k tile
+          SVDQ_TR(392, 8, j);
+          const uint32_t la = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+          const uint32_t lbp = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < RANK / 16; ++kk)
-              tc_mma_bf16(tmem, smem_desc(la + kk * 32, 16, 8 * C::LROW, C::LSW),
-                          smem_desc(lbp + kk * 32, 16, 8 * C::LROW, C::LSW), C::IDESC_BF16, 1u);
-            tc_commit_mc(&empty[s], kPairMask);
-            ++it;
-          } else {
-            ok = false;
+          for (int kk = 0; kk < RANK / 16; ++kk) {
+            tc_mma_bf16_pair_warp(tmem, smem_desc(la + kk * 32, 16, 8 * C::LROW, C::LSW),
+                                  smem_desc(lbp + kk * 32, 16, 8 * C::LROW, C::LSW),
+                                  C::IDESC_BF16, 1u);
+            if (kk == 0 && prev >= 0) release_slot(prev);
           }
+          release_slot(s);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        } else if (prev >= 0) {
+          release_slot(prev);
         }
-        if (!ok) *abort_flag = 1;
-        tc_commit(acc_full);  // fires once every MMA issued so far has completed
-        if (*abort_flag) break;
+        if (!ok) abort_pair();
+        // fires once every MMA issued so far has completed (in both CTAs)
+        tc_commit_pair_warp2(cluster_map(smem_u32(acc_full), 0u),
+                             cluster_map(smem_u32(acc_full), 1u));
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
       }
-      if (*abort_flag) tc_commit(acc_full);  // wake the epilogue after an abort
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {  // wake both epilogues after an abort
+        tc_commit_pair_warp2(cluster_map(smem_u32(acc_full), 0u),
+                             cluster_map(smem_u32(acc_full), 1u));
+      }
+      // no MMA may still write either TMEM when the pair frees it
+      tc_commit_pair_warp(cluster_map(smem_u32(mma_done), 0u));
+      mbar_wait(mma_done, 0u, dev_status, wait_ns);
     }
   } else if (warp >= SF_WARP0 && warp < SF_WARP0 + 4) {
     // ------------------------------------------------------------ scale warps
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     int it = 0;
+    // after this warp's TMEM stores (if any) are complete: one arrival on the
+    // even CTA's sf_full of the slot
+    auto report = [&](int s) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(at_even(&sf_full[s]));
+    };
     for (int j = 0; j < my_tiles; ++j) {
       bool ok = true;
       for (int kt = 0; kt < k_tiles; ++kt, ++it) {
@@ -487,12 +600,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               lds128(sfb + h * KB_PER_TILE * 512 + kb * 512));
         }
         tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&sf_full[s]);
+        report(s);
         if (warp == SF_WARP0 && lane == 0) SVDQ_TR(448, 128, it);
       }
       if (!ok) {
-        *abort_flag = 1;
+        abort_pair();
         break;
       }
       // the rank-r slot needs no scales; sf_full still completes once for it,
@@ -501,22 +613,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = mbar_wait(&full[s], (uint32_t)(it / STAGES) & 1u, dev_status, wait_ns) &&
            !*abort_flag;
       if (!__all_sync(0xFFFFFFFFu, ok)) {
-        *abort_flag = 1;
+        abort_pair();
         break;
       }
-      mbar_arrive(&sf_full[s]);
+      report(s);
       ++it;
     }
   } else if (warp >= EPI_WARP0) {
     // ------------------------------------------------------------ epilogue warps
     constexpr int CH = C::EPI_CH;
     const int q = warp & 3;  // TMEM lane quarter of this warp
-    const int col0 = ((warp - EPI_WARP0) >> 2) * C::EPI_COLS;
+    const int e = warp - EPI_WARP0;
+    const int col0 = (e >> 2) * C::EPI_COLS;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-    const int gbase = lane & ~(CH - 1), tc = lane & (CH - 1);
+    const uint32_t acc_empty_even = at_even(acc_empty);
+    // TMA-store epilogue: this warp's staging block; lane l writes row l, its
+    // 16-byte chunk c at byte offset o = l * ROW + 16 c XOR-ed with the
+    // swizzle of the output tensor map (bits 4.. of o ^= bits 7.. of o)
+    uint8_t* stage = smem + C::OFF_OUT + e * C::OUT_WARP_BYTES;
     // QKV: warps e and e ^ 4 hold the two 64-column halves of one head for the
     // same 32 rows; `pid` names the pair, `qk` counts its exchanges
-    const int e = warp - EPI_WARP0;
     const int pid = ((e >> 3) << 2) | (e & 3);
     int qk = 0;
     for (int j = 0; j < my_tiles; ++j) {
@@ -525,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m0 = m_tile * BM, n0 = n_tile * BN;
       bool ok = mbar_wait(acc_full, (uint32_t)(j & 1), dev_status, wait_ns) && !*abort_flag;
       if (!__all_sync(0xFFFFFFFFu, ok)) {
-        *abort_flag = 1;
+        abort_pair();
         break;
       }
       tc_fence_after();
@@ -538,11 +654,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(acc_empty);  // the accumulator is free for the next tile
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even);  // accumulator free for the next tile
       if (warp == EPI_WARP0 && lane == 0) SVDQ_TR(408, 8, j);
       if (warp == EPI_WARP0 + EPI_WARPS - 1 && lane == 0) SVDQ_TR(440, 8, j);
       // the bias slice landed with this tile's rank-r slot (the rank-r MMAs
-      // waited for it before acc_full was signalled)
+      // waited for it, through sf_full, before acc_full was signalled)
       const uint16_t* bsm =
           bias ? reinterpret_cast<const uint16_t*>(smem + C::OFF_BIAS + (j & 1) * C::BIAS_BYTES)
                : nullptr;
@@ -556,10 +673,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bias_empty[j & 1]);
       }
-      // QKV: 1/rms of this lane's row (before the transpose), used after it
-      float rs = 0.0f;
-      const int region = EPI == kEpiQkv ? (n0 < qe.hd ? 0 : (n0 < 2 * qe.hd ? 1 : 2)) : 2;
-      if constexpr (EPI == kEpiQkv) {
+      if constexpr (C::TMA_OUT) {
+        // rows at or past M are clipped by the tensor map (a block wholly past
+        // M is not stored at all)
+        constexpr int swz_mask = C::OUT_ROW_BYTES == 128 ? 7 : 3;  // 128B / 64B swizzle
+        if (lane == 0) bulk_wait_group_read0();  // the previous block left the staging area
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int o = lane * C::OUT_ROW_BYTES + 16 * c;
+          sts128(stage + (o ^ (((o >> 7) & swz_mask) << 4)), pk[4 * c], pk[4 * c + 1],
+                 pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();  // the generic-proxy writes, before the TMA engine reads them
+        __syncwarp();
+        if (lane == 0 && m0 + 32 * q < M) {
+          tma_store_2d(&tm_y, stage, n0 + col0, m0 + 32 * q);
+          bulk_commit_group();
+        }
+      } else {
+        const int gbase = lane & ~(CH - 1), tc = lane & (CH - 1);
+        // QKV: 1/rms of this lane's row (before the transpose), used after it
+        float rs = 0.0f;
+        const int region = n0 < qe.hd ? 0 : (n0 < 2 * qe.hd ? 1 : 2);
         if (region < 2) {  // a Q or K tile
           // sum of squares of this lane's 64 bf16 values (column order); the
           // partner's half arrives through shared memory
@@ -577,7 +713,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const bool got =
               mbar_wait(&pair_bar[pid], (uint32_t)(qk & 1), dev_status, wait_ns) && !*abort_flag;
           if (!__all_sync(0xFFFFFFFFu, got)) {
-            *abort_flag = 1;
+            abort_pair();
             break;
           }
           ++qk;
@@ -585,27 +721,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float total = (e & 4) ? other + ss : ss + other;  // lower columns first
           rs = rsqrtf(__fmaf_rn(total, 1.0f / kHeadDim, qe.eps));
         }
-      }
-      // after the transpose, store i of lane t writes chunk t % CH of row
-      // (t & ~(CH-1)) + i: CH consecutive lanes cover one row segment
-      transpose_chunks<CH>(pk, lane);
-      if constexpr (EPI == kEpiQkv) {
+        // after the transpose, store i of lane t writes chunk t % CH of row
+        // (t & ~(CH-1)) + i: CH consecutive lanes cover one row segment
+        transpose_chunks<CH>(pk, lane);
         if (region < 2)
           qkv_rotate_rows(pk, rs, gbase,
                           (region == 0 ? qe.norm_q : qe.norm_k) + (col0 & (kHeadDim - 1)) + 8 * tc,
                           qe.rope_cos, qe.rope_sin, m0 + 32 * q + gbase, M,
                           ((col0 & (kHeadDim - 1)) >> 1) + 4 * tc);
-      }
-      const int cbase = n0 + col0 + 8 * tc;
+        const int cbase = n0 + col0 + 8 * tc;
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int row = m0 + 32 * q + gbase + i;
-        if (row < M)
-          *reinterpret_cast<uint4*>(Y + (size_t)row * N + cbase) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < CH; ++i) {
+          const int row = m0 + 32 * q + gbase + i;
+          if (row < M)
+            *reinterpret_cast<uint4*>(Y + (size_t)row * N + cbase) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
       if (warp == EPI_WARP0 && lane == 0) SVDQ_TR(416, 8, j);
     }
+    // every TMA store of this warp has completed (and left its staging area)
+    if (C::TMA_OUT && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -615,12 +751,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = max(0, issued - STAGES); i < issued; ++i)
       mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u, nullptr, wait_ns);
   }
-  // neither CTA of the pair leaves while the other may still write its shared
-  // memory or arrive on its barriers
+  // neither CTA of the pair leaves (or frees TMEM) while the other may still
+  // write its shared memory, arrive on its barriers or run MMAs into its TMEM
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -648,8 +784,15 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query below takes the cluster shape only
   // persistent: as many CTA pairs as can be resident at once (a GPC with an
-  // odd number of free SMs leaves one idle), at most one per tile pair
-  static int max_pairs = 0;
+  // odd number of free SMs leaves one idle), at most one per tile pair; the
+  // count is queried once per device and instantiation
+  static std::atomic<int> max_pairs_of[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return cudaErrorInvalidDevice;
+  }
+  int max_pairs = max_pairs_of[dev].load(std::memory_order_relaxed);
   if (max_pairs == 0) {
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
     int n = 0;
@@ -657,14 +800,16 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
       cudaGetLastError();
       n = num_sms / 2;
     }
-    max_pairs = n;
+    max_pairs = n;  // every caller computes the same value: a plain store is enough
+    max_pairs_of[dev].store(n, std::memory_order_relaxed);
   }
   const int m_tiles = (M + BM - 1) / BM;
   const int pairs_needed = ((m_tiles + 1) / 2) * (N / BN);
   const int pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, maps.a_codes, maps.w_codes, maps.lora, maps.l2s, a_scales,
+  e = cudaLaunchKernelEx(&cfg, kern, maps.a_codes, maps.w_codes, maps.lora, maps.l2s, maps.y,
+                         a_scales,
                          w_scales, s_T, bias, Y, M, N, K, qe, dev_status, test_stall,
                          (uint64_t)(test_stall ? 100000000ull : kWaitTimeoutNs));
   if (e != cudaSuccess) return e;

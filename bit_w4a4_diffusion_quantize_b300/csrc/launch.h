@@ -15,12 +15,15 @@ cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                                 int* dev_status, cudaStream_t stream);
 
-// Tensor maps of svdq_gemm_w4a4 (and of its GELU variant).
+// Tensor maps of svdq_gemm_w4a4 (and of its GELU and QKV variants).  The
+// kernel runs on CTA pairs: each CTA loads its own 128 A rows and one half
+// (BN/2 rows) of the tile's W and L2s rows.
 struct GemmMaps {
   CUtensorMap a_codes;  // [M][K/2] bytes: box 128 x 128 rows, 128B swizzle
   CUtensorMap w_codes;  // [N][K/2] bytes: box 128 x BN/2 rows (one CTA's half), 128B swizzle
   CUtensorMap lora;     // lora_act [M][rank] bf16: box rank x 128 rows, swizzle = 2*rank bytes
-  CUtensorMap l2s;      // L2s [N][rank] bf16: box rank x BN rows, same swizzle
+  CUtensorMap l2s;      // L2s [N][rank] bf16: box rank x BN/2 rows, same swizzle
+  CUtensorMap y;        // Y [M][N] bf16: box BN/4 x 32 rows, swizzle = BN/2 bytes (stores)
 };
 
 // What svdq_gemm_w4a4's epilogue does after y = s_T * acc + bias is rounded to

@@ -7,6 +7,12 @@
 // mode 1: kind::f16 bf16 (M=128, N=n, K=16)
 // mode 2: mode 0 plus the tcgen05.cp of the scale chunks before every MMA
 //         (as the GEMM issues them)
+// mode 3: kind::mxf4nvf4 on CTA pairs (cta_group::2, M=256 over two SMs,
+//         N=n, K=64): clusters of two CTAs, the even one issues
+// mode 4: kind::f16 bf16 on CTA pairs (cta_group::2, M=256, N=n, K=16)
+// mode 5: mode 0 with consecutive MMAs alternating between two accumulators
+//         (n = 128: columns 0 and 128)
+// mode 6: mode 3 with the same alternation (n = 128)
 #include <cstdint>
 
 #include "../../include/svdq_bench.h"
@@ -60,9 +66,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_cp_32x128b_warpx4(sfb + 4 * h, smem_desc(sf + 512 * (h + 1), 128, 128,
                                                         kSwizzleNone));
         }
-        tc_mma_nvf4(tmem, smem_desc(a + koff, 16, 1024, kSwizzle128B),
+        const uint32_t d = mode == 5 ? tmem + (uint32_t)(i & 1) * 128u : tmem;
+        tc_mma_nvf4(d, smem_desc(a + koff, 16, 1024, kSwizzle128B),
                     smem_desc(b + koff, 16, 1024, kSwizzle128B), idesc_nvf4, sfa, sfb,
-                    i > 0 ? 1u : 0u);
+                    i > (mode == 5 ? 1 : 0) ? 1u : 0u);
       }
     }
     tc_commit(bar);
@@ -76,13 +83,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// modes 3 and 4: clusters of two CTAs; the pair allocates TMEM collectively,
+// the even CTA issues M=256 MMAs whose accumulator rows 128-255 live in the
+// odd CTA's TMEM and whose B operand is split between the two shared memories
+__global__ void __launch_bounds__(kThreads, 1)
+    k_mma_rate_pair(int mode, int n, int iters, int* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* A = smem;
+  uint8_t* B = smem + 16384;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(B + 32768 + 4096);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(B + 32768 + 4096 + 8);
+  for (int i = threadIdx.x; i < (16384 + 32768 + 4096) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  const int warp = threadIdx.x >> 5;
+  const uint32_t crank = cluster_ctarank();
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  cluster_sync();  // both CTAs resident before the collective allocation
+  if (warp == 0) tmem_alloc_pair(tslot, 512);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (crank == 0 && threadIdx.x == 0) {
+    const uint32_t a = smem_u32(A), b = smem_u32(B);
+    const uint32_t idesc_nvf4 =
+        (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    const uint32_t idesc_bf16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+    const uint32_t sfa = tmem + 256, sfb = tmem + 256 + 4;
+    for (int i = 0; i < iters; ++i) {
+      const uint32_t koff = (uint32_t)(i & 3) * 32;
+      if (mode == 4)
+        tc_mma_bf16_pair(tmem, smem_desc(a + koff, 16, 1024, kSwizzle128B),
+                         smem_desc(b + koff, 16, 1024, kSwizzle128B), idesc_bf16,
+                         i > 0 ? 1u : 0u);
+      else
+        tc_mma_nvf4_pair(mode == 6 ? tmem + (uint32_t)(i & 1) * 128u : tmem,
+                         smem_desc(a + koff, 16, 1024, kSwizzle128B),
+                         smem_desc(b + koff, 16, 1024, kSwizzle128B), idesc_nvf4, sfa, sfb,
+                         i > (mode == 6 ? 1 : 0) ? 1u : 0u);
+    }
+    tc_commit_pair(cluster_map(smem_u32(bar), 0));
+    mbar_wait(bar, 0, dev_status);
+  }
+  tc_fence_before();
+  cluster_sync();  // the pair's MMAs are complete before either CTA frees TMEM
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 }  // namespace
 }  // namespace svdq
 
 extern "C" svdq_status svdq_bench_mma_rate(int mode, int n, int iters, int ctas,
                                            int* dev_status, void* stream) {
-  if (mode < 0 || mode > 2 || (n != 128 && n != 256) || iters < 1 || ctas < 1)
+  if (mode < 0 || mode > 6 || (n != 128 && n != 256) || iters < 1 || ctas < 1)
     return SVDQ_ERR_SHAPE;
+  const bool pair = mode == 3 || mode == 4 || mode == 6;
+  if (pair && ctas % 2 != 0) return SVDQ_ERR_SHAPE;  // whole CTA pairs
+  if (mode >= 5 && n != 128) return SVDQ_ERR_SHAPE;  // two accumulators of 128 columns
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -92,6 +160,27 @@ extern "C" svdq_status svdq_bench_mma_rate(int mode, int n, int iters, int ctas,
   }
   if (major != 10 || minor != 3) return SVDQ_ERR_UNSUPPORTED_ARCH;
   const int smem = 16384 + 32768 + 4096 + 64 + 1024;
+  if (pair) {
+    if (cudaFuncSetAttribute(svdq::k_mma_rate_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return SVDQ_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(svdq::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, svdq::k_mma_rate_pair, mode, n, iters, dev_status) !=
+        cudaSuccess)
+      return SVDQ_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(svdq::k_mma_rate, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return SVDQ_ERR_CUDA;

@@ -247,7 +247,8 @@ svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
  * evaluated in fp32 (relative error below 2^-16 of the pair's norm), rounded
  * to nearest even once.
  * Inputs: norm_q, norm_k [128] bf16; rope_cos, rope_sin [M][64] fp32 (16-byte
- * aligned, caller-owned); eps >= 0 and finite (SVDQ_ERR_VALUE otherwise).
+ * aligned, caller-owned); eps > 0 and finite (SVDQ_ERR_VALUE otherwise: with
+ * eps = 0 an all-zero head would give 0 * inf).
  * Output: QKV [M][N] bf16.  Sizes: N % 768 == 0 (SVDQ_ERR_SHAPE otherwise);
  * everything else as svdq_gemm_w4a4. */
 svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,

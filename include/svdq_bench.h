@@ -13,8 +13,16 @@
  *   mode 1: kind::f16 (bf16 inputs, fp32 accumulate), K_mma = 16
  *   mode 2: mode 0 plus the tcgen05.cp copies of the block-scale chunks
  *           (1 + n/128 of them) before every MMA, as the GEMM issues them
+ *   mode 3: mode 0 on CTA pairs (tcgen05 cta_group::2: clusters of two CTAs,
+ *           one M = 256 MMA over the two SMs, issued by the even CTA)
+ *   mode 4: mode 1 on CTA pairs (cta_group::2, M = 256)
+ *   mode 5: mode 0 with consecutive MMAs alternating between two
+ *           accumulators (n = 128 only)
+ *   mode 6: mode 3 with the same alternation (n = 128 only)
+ * For modes 3, 4 and 6 the work is 2 * 256 * n * K_mma * iters * ctas / 2
+ * flops, the same total as the formula above.
  *
- * n in {128, 256}; iters >= 1; ctas >= 1.  dev_status (nullable device int)
+ * n in {128, 256}; iters >= 1; ctas >= 1 (even for modes 3, 4 and 6).  dev_status (nullable device int)
  * receives SVDQ_DEV_TIMEOUT if the completion wait exceeds its bound.
  * Errors: SVDQ_ERR_SHAPE, SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA.
  * The pages have no counterpart: this is instrumentation for the roofline.

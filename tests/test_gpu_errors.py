@@ -1,8 +1,8 @@
 """Device-side error behaviour through the C ABI: the compute-capability
-check (forced with the host test hook SVDQ_FAKE_COMPUTE_CAPABILITY), pointer
-alignment checks on real device buffers, empty inputs, and the bounded
-pipeline wait of the GEMM (forced with SVDQ_TEST_GEMM_STALL: the loader
-issues nothing, the wait runs out after 100 ms, the kernel reports
+check (forced with the library's test hook svdq_test_set_hooks: a reported
+capability of 9.0), pointer alignment checks on real device buffers, empty
+inputs, and the bounded pipeline waits of the GEMM (forced with the same hook:
+the loader issues nothing, the waits run out after 100 ms, the kernel reports
 SVDQ_DEV_TIMEOUT through dev_status and returns; the context stays usable).
 No test here faults or hangs the GPU."""
 import ctypes
@@ -35,20 +35,22 @@ def test_device_is_supported():
     assert lib.check_device() == 0
 
 
-def test_fake_capability_is_refused(monkeypatch):
+def test_fake_capability_is_refused():
     case, X, b, packed, out, w = _small_problem()
-    monkeypatch.setenv("SVDQ_FAKE_COMPUTE_CAPABILITY", "9.0")
-    assert lib.check_device() == -4
-    with pytest.raises(lib.SvdqError) as e:
-        lib.svdq_quantize_act(dev_bf16(X), w["inv_lambda"], w["L1s"], 16)
-    assert e.value.status == -4
-    Xa = torch.zeros((1, 256), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(lib.SvdqError) as e:
-        lib.awq_gemv_w4a16(Xa, torch.zeros((64, 128), dtype=torch.uint8, device="cuda"),
-                           torch.zeros((64, 4), dtype=torch.float16, device="cuda"),
-                           torch.zeros((64, 4), dtype=torch.float16, device="cuda"), None)
-    assert e.value.status == -4
-    monkeypatch.delenv("SVDQ_FAKE_COMPUTE_CAPABILITY")
+    lib.test_set_hooks(fake_compute_capability=90)
+    try:
+        assert lib.check_device() == -4
+        with pytest.raises(lib.SvdqError) as e:
+            lib.svdq_quantize_act(dev_bf16(X), w["inv_lambda"], w["L1s"], 16)
+        assert e.value.status == -4
+        Xa = torch.zeros((1, 256), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(lib.SvdqError) as e:
+            lib.awq_gemv_w4a16(Xa, torch.zeros((64, 128), dtype=torch.uint8, device="cuda"),
+                               torch.zeros((64, 4), dtype=torch.float16, device="cuda"),
+                               torch.zeros((64, 4), dtype=torch.float16, device="cuda"), None)
+        assert e.value.status == -4
+    finally:
+        lib.test_set_hooks()
     assert lib.check_device() == 0
 
 
@@ -77,18 +79,20 @@ def test_dev_status_stays_clear_and_empty_input_is_a_no_op():
                        None, 0, 256, 256, 16, Y=Y0)
 
 
-def test_gemm_pipeline_wait_times_out_cleanly(monkeypatch):
+def test_gemm_pipeline_wait_times_out_cleanly():
     case, X, b, packed, out, w = _small_problem()
     a_codes = dev_u8(out["a_codes_packed"])
     a_scales = dev_u8(out["a_scales_swizzled"])
     lora = dev_bits16(formats.bf16_bits(out["lora_act"]))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    monkeypatch.setenv("SVDQ_TEST_GEMM_STALL", "1")
-    lib.svdq_gemm_w4a4(a_codes, a_scales, w["w_codes"], w["w_scales"], w["s_T"], lora, w["L2"],
-                       w["bias"], 64, 256, 256, 16, dev_status=status)
-    torch.cuda.synchronize()
+    lib.test_set_hooks(gemm_stall=1)
+    try:
+        lib.svdq_gemm_w4a4(a_codes, a_scales, w["w_codes"], w["w_scales"], w["s_T"], lora,
+                           w["L2"], w["bias"], 64, 256, 256, 16, dev_status=status)
+        torch.cuda.synchronize()
+    finally:
+        lib.test_set_hooks()
     assert int(status.item()) == lib.DEV_TIMEOUT
-    monkeypatch.delenv("SVDQ_TEST_GEMM_STALL")
     # the context is intact: the same call now completes and is correct
     status.zero_()
     Y = lib.svdq_gemm_w4a4(a_codes, a_scales, w["w_codes"], w["w_scales"], w["s_T"], lora,

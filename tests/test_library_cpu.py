@@ -44,6 +44,13 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(raw, n), n
 
 
+def test_test_hooks_refuse_bad_values_and_reset():
+    raw = lib.raw_lib()
+    assert raw.svdq_test_set_hooks(-1, 0) == -7
+    assert raw.svdq_test_set_hooks(0, 2) == -7
+    assert raw.svdq_test_set_hooks(0, 0) == 0
+
+
 def test_status_strings():
     for st in range(-8, 1):
         s = lib.raw_lib().svdq_status_string(st).decode()
@@ -111,6 +118,7 @@ def test_qkv_argument_errors():
     assert _qkv(N=512) == -2 and _qkv(N=1152) == -2      # not whole pairs of 128-wide heads
     assert _qkv(r=8) == -6
     assert _qkv(eps=-1e-6) == -7 and _qkv(eps=float("nan")) == -7 and _qkv(eps=float("inf")) == -7
+    assert _qkv(eps=0.0) == -7   # an all-zero head would give 0 * rsqrt(0) = NaN
     assert _qkv(nq=P(0)) == -1 and _qkv(cos=P(0)) == -1
     assert _qkv(cos=MISALIGNED) == -3 and _qkv(nq=MISALIGNED) == -3
     assert _qkv(M=0, nq=P(0)) == 0
