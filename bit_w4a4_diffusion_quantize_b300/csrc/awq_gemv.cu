@@ -122,6 +122,23 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
     abort_flag = 0;
     fence_mbar_init();
   }
+  // The weights of this CTA's tiles are read-only operands: ask L2 for all of
+  // them now (hints only, no data comes back), before the wait for the
+  // previous kernel, so that the stream from HBM starts with the launch and
+  // the loads below find L2 lines.
+  if (threadIdx.x == 32 * CW) {
+    const size_t row_bytes = (size_t)K / 2;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int n0 = (blockIdx.x + j * gridDim.x) * 16;
+      const int rows = min(16, N - n0);
+      bulk_prefetch_l2(qw + (size_t)n0 * row_bytes, (uint32_t)(rows * row_bytes));
+      const uint32_t gb = (uint32_t)(rows * G * 2) & ~15u;  // whole 16-byte pieces
+      if (gb) {
+        bulk_prefetch_l2(sc + (size_t)n0 * G, gb);
+        bulk_prefetch_l2(zr + (size_t)n0 * G, gb);
+      }
+    }
+  }
   __syncthreads();
   grid_dep_launch();
   grid_dep_wait();  // the previous kernel's outputs (X among them) are complete

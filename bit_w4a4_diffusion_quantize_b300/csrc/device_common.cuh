@@ -240,6 +240,11 @@ SVDQ_DEVINL void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
+// hint: bring `bytes` (a multiple of 16, 16-byte aligned) at p into L2; no
+// data is returned to the issuing CTA and nothing waits for it
+SVDQ_DEVINL void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 // hint: bring the 128-byte line at p into L2 (no data returned)
 SVDQ_DEVINL void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
