@@ -41,6 +41,7 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "SVDQ W4A4 NVFP4 linear TFLOP/s & % FP4 tensor peak; AWQ W4A16 HBM GB/s"
+_SAMPLE = {}  # device output rows kept for the quality figures
 L2_BYTES = 126 * 1024 * 1024
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
 
@@ -203,6 +204,28 @@ def time_oracle(case, sample_rows: int, steps: int):
     return statistics.median(ts), 2.0 * sample_rows * case.N * case.K, os.cpu_count()
 
 
+def quality_sample(case, rows: int, y_dev_rows):
+    """The quality invariant on the first `rows` rows of the workload: relative
+    Frobenius error against float64 X W^T + b of the device's SVDQ output, of
+    smoothing alone (no low-rank branch) and of plain W4A4 (neither), the
+    latter two by the oracle with the same NVFP4 rules."""
+    from oracle import svdq
+    X_full = workloads.make_activations(case)
+    X = X_full[:rows]
+    W, b = workloads.make_weights(case)
+    exact = X.astype(np.float64) @ W.T.astype(np.float64) + b
+    nrm = np.linalg.norm(exact)
+    smooth = svdq.linear_forward(X, svdq.pack_weights(W, svdq.calib_absmax(X_full), 0), b)["Y"]
+    naive = svdq.naive_w4a4(X, W, b)
+    e = {"svdq_device": float(np.linalg.norm(y_dev_rows - exact) / nrm),
+         "smoothing_only": float(np.linalg.norm(smooth - exact) / nrm),
+         "naive_w4a4": float(np.linalg.norm(naive - exact) / nrm)}
+    return {"sample": f"first {rows} of {case.M} rows of the {case.name} workload",
+            "rel_fro_err_vs_fp64": {k: round(v, 5) for k, v in e.items()},
+            "svdq_below_naive": e["svdq_device"] < e["naive_w4a4"],
+            "svdq_below_smoothing_only": e["svdq_device"] < e["smoothing_only"]}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_gpu(args, world, rank, local):
     import torch
@@ -284,6 +307,16 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e-3
 
+    def repeated(g, reps):
+        """`reps` timed replays of a graph of exactly `steps` launches, each
+        bracketed by barrier + synchronize; seconds per replay."""
+        ts = []
+        for _ in range(reps):
+            barrier(world)
+            torch.cuda.synchronize()
+            ts.append(timed(g))
+        return ts
+
     for i in range(args.warmup):            # eager warm-up: module load, every set written
         step(i, stream)
     torch.cuda.synchronize()
@@ -295,11 +328,15 @@ def run_gpu(args, world, rank, local):
         barrier(world)
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
-        t_total = timed(g_step)               # the timed region: exactly `steps` steps
+        # the timed region: `reps` replays of exactly `steps` steps each
+        ts_step = repeated(g_step, args.reps)
         wall = time.perf_counter() - wall0
         barrier(world)
-        t_q = timed(g_q) / args.steps
-        t_g = timed(g_g) / args.steps
+        ts_q = repeated(g_q, args.reps)
+        ts_g = repeated(g_g, args.reps)
+        t_total = statistics.median(ts_step)
+        t_q = statistics.median(ts_q) / args.steps
+        t_g = statistics.median(ts_g) / args.steps
         # keep the same load running so the clock record spans >= clock_window s
         t_end = time.perf_counter() + max(0.0, args.clock_window - (time.perf_counter() - wall0))
         while time.perf_counter() < t_end:
@@ -307,6 +344,9 @@ def run_gpu(args, world, rank, local):
             torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError("device status set during the timed region")
+    # device output rows for the quality figures (every set holds the same X)
+    _SAMPLE["y_rows"] = sets[0]["Y"][:args.oracle_rows].view(torch.int16).cpu().numpy().view(
+        np.uint16)
     t_total = max_over_ranks(t_total, world, dev)
     flop = 2.0 * M * N * K
     value = world * args.steps * flop / t_total / 1e12
@@ -418,9 +458,14 @@ def run_gpu(args, world, rank, local):
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in e2e.items()},
         "e2e_pipelined": {k: (round(v, 3) if isinstance(v, float) else v)
                           for k, v in e2e_pipe.items()},
-        "gpu_launches": 2 * args.steps,
-        "timing": "CUDA graph of the steps, CUDA events around its replay; per-kernel times "
-                  "from graphs of that kernel alone",
+        "gpu_launches": 2 * args.steps * args.reps,
+        "timing": f"median of {args.reps} replays of a CUDA graph of the {args.steps} steps "
+                  "(CUDA events around each replay, barrier + synchronize on both sides); "
+                  "per-kernel times the same way from graphs of that kernel alone",
+        "spread": {"replays": args.reps,
+                   "step_us": _spread([t / args.steps for t in ts_step]),
+                   "svdq_quantize_act_us": _spread([t / args.steps for t in ts_q]),
+                   "svdq_gemm_w4a4_us": _spread([t / args.steps for t in ts_g])},
         "clocks": clk.summary(),
         "pack_seconds": round(pack_s, 2),
         "wall_s_timed": round(wall, 4),
@@ -439,6 +484,12 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+def _spread(ts):
+    """min / 10th percentile / median / 90th percentile / max, microseconds."""
+    q = np.percentile(np.asarray(ts) * 1e6, [0, 10, 50, 90, 100])
+    return {k: round(float(v), 3) for k, v in zip(("min", "p10", "median", "p90", "max"), q)}
+
+
 def _time_graph(args, launch, fn, stream, dev, world):
     """Per-launch seconds of `args.steps` launches of fn captured in a CUDA
     graph (eager warm-up first), max over ranks."""
@@ -453,12 +504,15 @@ def _time_graph(args, launch, fn, stream, dev, world):
             launch(fn, i, cs)
     g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world, dev)
+    ts = []
+    for _ in range(max(1, min(args.reps, 20))):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3 / args.steps)
+    return max_over_ranks(statistics.median(ts), world, dev)
 
 
 def run_qkv_epilogue(args, lib, dev, stream, world):
@@ -557,22 +611,7 @@ def run_mlp_gelu(args, lib, dev, stream, world):
     res = {"workload": f"fc1: SVDQ W4A4 linear + GELU (tanh) M={M} K={K} N={N} rank={r}",
            "launches": 0}
     for name, fn in (("gelu", lib.svdq_gemm_w4a4_gelu), ("plain", lib.svdq_gemm_w4a4)):
-        for i in range(args.warmup):
-            launch(fn, i, stream)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            cs = torch.cuda.current_stream(dev)
-            for i in range(args.steps):
-                launch(fn, i, cs)
-        g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, world, dev)
+        t = _time_graph(args, launch, fn, stream, dev, world)
         res[f"us_{name}"] = round(t * 1e6, 2)
         res[f"tflops_{name}"] = round(world * 2.0 * M * N * K / t / 1e12, 1)
         res["launches"] += args.steps
@@ -713,6 +752,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=50,
+                    help="timed replays of the K-step graph (the median is reported)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="attn_out", choices=sorted(workloads.CASES))
     ap.add_argument("--awq-blocks", type=int, default=workloads.AWQ_BLOCKS)
@@ -745,6 +786,10 @@ def main(argv=None):
                 "kind": "oracle",
                 "sample": f"{args.oracle_rows} of {case.M} rows per step, median of 3 "
                           "(oracle packing not timed)"}
+            if "y_rows" in _SAMPLE:
+                y = (_SAMPLE["y_rows"].astype(np.uint32) << 16).view(np.float32).astype(
+                    np.float64)
+                line["quality"] = quality_sample(case, args.oracle_rows, y)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

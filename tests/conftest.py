@@ -22,3 +22,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "slow" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The output checks' unmodified error figures and how many elements each
+    widening of the 1e-2 * rms(Y) bound admitted (tests/gpu_util.py)."""
+    mod = sys.modules.get("gpu_util")
+    log = getattr(mod, "TOLERANCE_LOG", None) if mod else None
+    if not log:
+        return
+    tr = terminalreporter
+    tr.section("output tolerance book-keeping")
+    tr.write_line(f"{'check':44s} {'elements':>10s} {'rel_fro':>9s} {'max|err|/rms':>12s} "
+                  f"{'>1e-2rms':>9s} {'>+ulp/2':>8s}")
+    for r in log:
+        tr.write_line(f"{r['what'][:44]:44s} {r['elements']:10d} {r['rel_fro']:9.2e} "
+                      f"{r['max_abs_over_rms']:12.4f} {r['needed_half_ulp']:9d} "
+                      f"{r['needed_lora_slack']:8d}")

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import workloads
-from oracle import formats, svdq
+from oracle import formats, layout, svdq
 
 import bit_w4a4_diffusion_quantize_b300 as lib
 from gpu_util import (assert_y_close, dev_bf16, host_bf16, lora_rounding_slack,
@@ -71,6 +71,44 @@ def test_mlp_pair_fc1_gelu_fc2():
     _, _, _, p2, o2 = _oracle_case(c2, X2, W2, b2)
     Y2, _, _, _ = _device_forward(X2, oracle_weight_operands(p2, b2), c2.rank)
     assert_y_close(host_bf16(Y2), o2["Y"], "fc2", _slack(X2, p2))
+
+
+def _oracle_view_of_product_packing(p):
+    """The oracle's packed-weight dict for weights packed by svdq_pack_weights:
+    its smoothing, bf16 factors (L2 = L2s^T s_T, exact), codes and scales."""
+    N, K = p["N"], p["K"]
+    return {"N": N, "K": K, "rank": p["rank"], "inv_lambda": p["inv_lambda"],
+            "L1s": formats.bf16_from_bits(p["L1s"]).T,
+            "L2": formats.bf16_from_bits(p["L2s"]).T * p["w_tensor_scale"],
+            "s_T": p["w_tensor_scale"],
+            "w_codes": layout.unpack_nibbles(p["w_codes"]).reshape(N, K),
+            "w_scales": layout.sf_unswizzle(p["w_scales"], N, K // 16),
+            "factor_rounding": "bf16"}
+
+
+def test_product_packer_parity_attn_out():
+    """The attention out-projection (M = 4096, K = N = 3072, rank 32) with the
+    weights packed by svdq_pack_weights (not the oracle): the device forward
+    against the oracle's forward on those same packed weights, every code
+    and every output."""
+    case = workloads.CASES["attn_out"]
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    p = lib.svdq_pack_weights(W, lib.svdq_calib_absmax(workloads.bf16_bits_of(X)), case.rank)
+    view = _oracle_view_of_product_packing(p)
+    out = svdq.linear_forward(X, view, b)
+    layer = lib.SVDQLinear(p, workloads.bf16_bits_of(b))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, lora = lib.svdq_quantize_act(dev_bf16(X), layer.inv_lambda, layer.L1s,
+                                                case.rank, dev_status=status)
+    Y = lib.svdq_gemm_w4a4(codes, scales, layer.w_codes, layer.w_scales, layer.w_tensor_scale,
+                           lora, layer.L2s, layer.bias, case.M, case.N, case.K, case.rank,
+                           dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(codes.cpu().numpy(), layout.pack_nibbles(out["a_codes"]))
+    assert_y_close(host_bf16(Y), out["Y"], "attn_out, product packer",
+                   lora_rounding_slack(X, view["L1s"], view["L2"]))
 
 
 def test_product_packer_quality_through_device():
