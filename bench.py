@@ -51,20 +51,19 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
 # sources hash to what was captured (the summaries are under profiles/).
 MEASURED_TRAFFIC = {
     "svdq_gemm_w4a4": {
-        "bytes": 12890368 + 7936,
-        "sources": {"gemm_w4a4.cu": "7c27d67a54caad6252a81852cd1425506068d7b621ebb7d639e80f08a9c89b01",
-                    "device_common.cuh": "14fcfcad0223e45a87c376a282b794f821e828b7c0b6681df40e12e424363a88"},
-        "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md",
-        "note": "captured before the GELU epilogue variant was added to gemm_w4a4.cu"},
+        "bytes": 12889600 + 3840,
+        "sources": {"gemm_w4a4.cu": "d7ad3de4a2d5ad21afa9c7fa13715414b78b00ae06f82425dbee6f2e00f65dc7",
+                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
+        "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
     "svdq_quantize_act": {
-        "bytes": 25392128 + 0,
+        "bytes": 25391616 + 0,
         "sources": {"quantize_act.cu": "1ac727eb664eed2921ff4941ba6decbc109f896b8bda3fa0f110429d2869aac9",
-                    "device_common.cuh": "14fcfcad0223e45a87c376a282b794f821e828b7c0b6681df40e12e424363a88"},
+                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
         "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
-        "bytes": 31931648 + 0,
-        "sources": {"awq_gemv.cu": "bfe4b6a3c3f6d8fa081b186ad6a4e3c72fbae4de903745a2a41da36db5f96c5a",
-                    "device_common.cuh": "14fcfcad0223e45a87c376a282b794f821e828b7c0b6681df40e12e424363a88"},
+        "bytes": 31935488 + 0,
+        "sources": {"awq_gemv.cu": "59c214c33078bf99e64d0086c8b1bb568d561ed08180de56c4fe71080abba856",
+                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
         "profile": "profiles/awq_gemv_w4a16_modulation_ncu.md"},
 }
 
