@@ -618,6 +618,51 @@ def run_mlp_gelu(args, lib, dev, stream, world):
         raise RuntimeError("device status set during the fc1 GELU phase")
     res["gelu_epilogue_cost"] = round(res["us_gelu"] / res["us_plain"] - 1.0, 4)
     res["separate_gelu_bytes_avoided"] = 2 * M * N * 2
+
+    # fc2's activation side (K2 = N, rank 32) fused as well
+    # (svdq_gemm_w4a4_gelu_quant, H not written), against fc1 + GELU followed by
+    # svdq_quantize_act on H.  fc2's smoothing and down-projection factor are
+    # synthetic here (inv_lambda2 = 2^u, u ~ U(-3, 3); L1s2 ~ N(0, 0.05^2) in
+    # bf16): the kernels' work does not depend on their values.
+    r2 = workloads.CASES["fc2"].rank
+    rng = np.random.default_rng(77)
+    inv2 = torch.from_numpy(np.exp2(rng.uniform(-3.0, 3.0, N)).astype(np.float32)).to(dev)
+    l1s2 = dbits(workloads.bf16_bits_of(
+        workloads.to_bf16_values(rng.standard_normal((r2, N)) * 0.05)))
+    for s in sets:
+        s["a2c"] = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+        s["a2s"] = torch.empty(lib.scale_bytes(M, N), dtype=torch.uint8, device=dev)
+        s["l2"] = torch.empty((M, r2), dtype=torch.bfloat16, device=dev)
+        s["scr"] = torch.empty(lib.gelu_quant_scratch_bytes(M, N, r2), dtype=torch.uint8,
+                               device=dev)
+
+    def fused_quant(s, st):
+        lib.svdq_gemm_w4a4_gelu_quant(s["ac"], s["as"], s["wc"], s["ws"],
+                                      packed["w_tensor_scale"], s["lora"], s["L2s"], s["bias"],
+                                      inv2, l1s2, r2, M, N, K, r, a2_codes=s["a2c"],
+                                      a2_scales=s["a2s"], lora_act2=s["l2"], scratch=s["scr"],
+                                      dev_status=status, stream=st)
+
+    def gelu_then_quant(s, st):
+        lib.svdq_gemm_w4a4_gelu(s["ac"], s["as"], s["wc"], s["ws"], packed["w_tensor_scale"],
+                                s["lora"], s["L2s"], s["bias"], M, N, K, r, s["Y"],
+                                dev_status=status, stream=st)
+        lib.svdq_quantize_act(s["Y"], inv2, l1s2, r2, s["a2c"], s["a2s"], s["l2"],
+                              dev_status=status, stream=st)
+
+    def launch2(fn, i, st):
+        fn(sets[i % len(sets)], st)
+
+    for name, fn in (("gelu_quant", fused_quant), ("gelu_then_quantize_act", gelu_then_quant)):
+        t = _time_graph(args, launch2, fn, stream, dev, world)
+        res[f"us_{name}"] = round(t * 1e6, 2)
+        res["launches"] += 2 * args.steps
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the fc1 GELU + quantization phase")
+    res["gelu_quant_workload"] = (f"fc1 + GELU + fc2 activation quantization and down "
+                                  f"projection (K2={N}, rank2={r2})")
+    res["gelu_quant_saving"] = round(1.0 - res["us_gelu_quant"] /
+                                     res["us_gelu_then_quantize_act"], 4)
     return res
 
 

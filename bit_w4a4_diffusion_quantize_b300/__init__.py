@@ -13,7 +13,7 @@ _LIB_NAMES = {
     "DEV_OK", "DEV_TIMEOUT", "LIB_PATH", "SvdqError", "awq_gemv_w4a16", "awq_pack_weights",
     "bench_mma_rate", "check_device", "code_bytes", "raw_lib", "scale_bytes", "status_name",
     "svdq_calib_absmax", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu", "svdq_gemm_w4a4_qkv",
-    "svdq_pack_weights",
+    "svdq_gemm_w4a4_gelu_quant", "gelu_quant_scratch_bytes", "svdq_pack_weights",
     "svdq_quantize_act", "test_set_hooks",
 }
 _LAYER_NAMES = {"SVDQLinear", "AWQLinear"}

@@ -50,6 +50,9 @@ _SIGS = {
                                    _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "svdq_gemm_w4a4_qkv": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _c_p,
                                   _c_p, _c_p, _f32, _c_p, _i32, _i32, _i32, _i32, _c_p, _c_p]),
+    "svdq_gemm_w4a4_gelu_quant": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p,
+                                         _c_p, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                         ctypes.c_size_t, _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
@@ -89,6 +92,11 @@ def code_bytes(rows: int, K: int) -> int:
 
 def scale_bytes(rows: int, K: int) -> int:
     return ((rows + 127) // 128) * 128 * (K // 16)
+
+
+def gelu_quant_scratch_bytes(M: int, N: int, rank2: int) -> int:
+    """Scratch svdq_gemm_w4a4_gelu_quant needs (SVDQ_GELU_QUANT_SCRATCH_BYTES)."""
+    return (128 + (M + 255) // 256) * 256 * rank2 * 4
 
 
 # --------------------------------------------------------------------------- host calls
@@ -294,6 +302,56 @@ def svdq_gemm_w4a4_qkv(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: flo
                                  _stream_ptr(stream))
     _check(st, "svdq_gemm_w4a4_qkv")
     return QKV
+
+
+def svdq_gemm_w4a4_gelu_quant(a_codes, a_scales, w_codes, w_scales, w_tensor_scale: float,
+                              lora_act, L2s, bias, inv_lambda2, L1s2, rank2: int, M: int, N: int,
+                              K: int, rank: int, a2_codes=None, a2_scales=None, lora_act2=None,
+                              H=None, scratch=None, dev_status=None, stream=None):
+    """svdq_gemm_w4a4_gelu with the next SVDQ linear's activation side fused:
+    returns (a2_codes, a2_scales, lora_act2) of H = bf16(gelu_tanh(Y)) for the
+    layer with inv_lambda2 [N] fp32 and L1s2 bf16 bits [rank2, N]; H [M, N]
+    bf16 is written only when passed.  `scratch` (uint8/float, CUDA) holds at
+    least gelu_quant_scratch_bytes(M, N, rank2) bytes (allocated if None)."""
+    torch = _torch()
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias"),
+                 (inv_lambda2, "inv_lambda2"), (L1s2, "L1s2"), (a2_codes, "a2_codes"),
+                 (a2_scales, "a2_scales"), (lora_act2, "lora_act2"), (H, "H"),
+                 (scratch, "scratch"), (dev_status, "dev_status")):
+        _check_cuda(t, n)
+    dev = a_codes.device
+    if a2_codes is None:
+        a2_codes = torch.empty((M, N // 2), dtype=torch.uint8, device=dev)
+    if a2_scales is None:
+        a2_scales = torch.empty(scale_bytes(M, N), dtype=torch.uint8, device=dev)
+    if lora_act2 is None:
+        lora_act2 = torch.empty((M, rank2), dtype=torch.bfloat16, device=dev)
+    need = gelu_quant_scratch_bytes(M, N, rank2)
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if M > 0:
+        for t, n, e, z in ((a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", scale_bytes(M, K), 1),
+                           (w_codes, "w_codes", code_bytes(N, K), 1),
+                           (w_scales, "w_scales", scale_bytes(N, K), 1),
+                           (lora_act, "lora_act", M * rank, 2), (L2s, "L2s", N * rank, 2),
+                           (bias, "bias", N, 2), (inv_lambda2, "inv_lambda2", N, 4),
+                           (L1s2, "L1s2", rank2 * N, 2),
+                           (a2_codes, "a2_codes", code_bytes(M, N), 1),
+                           (a2_scales, "a2_scales", scale_bytes(M, N), 1),
+                           (lora_act2, "lora_act2", M * rank2, 2), (H, "H", M * N, 2),
+                           (dev_status, "dev_status", 1, 4)):
+            _need(t, n, e, z)
+    scratch_bytes = scratch.numel() * scratch.element_size()
+    st = _lib.svdq_gemm_w4a4_gelu_quant(
+        _dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales), float(w_tensor_scale),
+        _dptr(lora_act), _dptr(L2s), _dptr(bias), _dptr(inv_lambda2), _dptr(L1s2), int(rank2),
+        _dptr(a2_codes), _dptr(a2_scales), _dptr(lora_act2), _dptr(H), _dptr(scratch),
+        int(scratch_bytes), int(M), int(N), int(K), int(rank), _dptr(dev_status),
+        _stream_ptr(stream))
+    _check(st, "svdq_gemm_w4a4_gelu_quant")
+    return a2_codes, a2_scales, lora_act2
 
 
 def awq_gemv_w4a16(X, qweight, scales, zeros, bias, group_size: int = 64, Y=None,

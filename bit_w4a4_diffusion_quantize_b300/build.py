@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu", "microbench.cu"]
 HOST_SOURCES = ["pack.cpp"]
-HEADERS = ["device_common.cuh", "launch.h"]
+HEADERS = ["device_common.cuh", "act_quant.cuh", "launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

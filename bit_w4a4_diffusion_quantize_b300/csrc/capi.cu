@@ -180,11 +180,15 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
                       const uint8_t* w_scales, float w_tensor_scale, const uint16_t* lora_act,
                       const uint16_t* L2s, const uint16_t* bias, uint16_t* Y, int M, int N,
                       int K, int rank, svdq::GemmEpilogue epi, const svdq::QkvEpilogue& qe,
+                      const svdq::GeluQuantEpilogue& gq, const uint16_t* L1s2,
                       int* dev_status, void* stream) {
+  const bool is_gq = epi == svdq::GemmEpilogue::kGeluQuant;
   const bool is_qkv = epi == svdq::GemmEpilogue::kQkv;
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
   if (is_qkv && N % 768 != 0) return SVDQ_ERR_SHAPE;  // Q, K, V: whole pairs of 128-wide heads
+  if (is_gq && N % 256 != 0) return SVDQ_ERR_SHAPE;
   if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  if (is_gq && gq.rank2 != 32 && gq.rank2 != 64) return SVDQ_ERR_RANK;
   if (is_qkv && !(std::isfinite(qe.eps) && qe.eps > 0.0f)) return SVDQ_ERR_VALUE;
   {
     // a finite power of two in [2^-100, 2^100]
@@ -194,13 +198,24 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
       return SVDQ_ERR_VALUE;
   }
   if (M == 0) return SVDQ_OK;
-  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2s || !Y)
+  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2s || (!Y && !is_gq))
     return SVDQ_ERR_NULL;
+  if (is_gq && (!gq.inv_lambda2 || !L1s2 || !gq.a2_codes || !gq.a2_scales || !gq.lora2 ||
+                !gq.partial))
+    return SVDQ_ERR_NULL;
+  if (is_gq && gq.scratch_bytes < SVDQ_GELU_QUANT_SCRATCH_BYTES(M, N, gq.rank2))
+    return SVDQ_ERR_SHAPE;
+  // (the segment bookkeeping multiplies tile counts by the pair count in 32 bits)
+  if (is_gq && ((size_t)M + 255) / 256 * (size_t)(N / 256) * 128 >= ((size_t)1 << 31))
+    return SVDQ_ERR_SHAPE;
   if (is_qkv && (!qe.norm_q || !qe.norm_k || !qe.rope_cos || !qe.rope_sin))
     return SVDQ_ERR_NULL;
   if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
-      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2s) || !aligned16(Y) ||
+      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2s) || (Y && !aligned16(Y)) ||
       (bias && !aligned16(bias)))
+    return SVDQ_ERR_ALIGN;
+  if (is_gq && (!aligned16(gq.inv_lambda2) || !aligned16(L1s2) || !aligned16(gq.a2_codes) ||
+                !aligned16(gq.a2_scales) || !aligned16(gq.lora2) || !aligned16(gq.partial)))
     return SVDQ_ERR_ALIGN;
   if (is_qkv && (!aligned16(qe.norm_q) || !aligned16(qe.norm_k) || !aligned16(qe.rope_cos) ||
                  !aligned16(qe.rope_sin)))
@@ -214,15 +229,24 @@ svdq_status gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales, const uin
       !encode_codes(&maps.w_codes, w_codes, N, K, block_n / 2) ||
       !encode_rank_rows(&maps.lora, lora_act, M, rank, 128) ||
       !encode_rank_rows(&maps.l2s, L2s, N, rank, block_n / 2) ||
-      !encode_2d(&maps.y, CU_TENSOR_MAP_DATA_TYPE_UINT16, Y, (uint64_t)N, (uint64_t)M,
-                 (uint64_t)N * 2, (uint32_t)(block_n / 4), 32u,
-                 block_n == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      (Y && !encode_2d(&maps.y, CU_TENSOR_MAP_DATA_TYPE_UINT16, Y, (uint64_t)N, (uint64_t)M,
+                       (uint64_t)N * 2, (uint32_t)(block_n / 4), 32u,
+                       block_n == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)))
     return SVDQ_ERR_CUDA;
+  if (!Y) std::memset(&maps.y, 0, sizeof(maps.y));  // GELU + quantization without H: unused
+  if (is_gq) {
+    if (!encode_2d(&maps.l1s2, CU_TENSOR_MAP_DATA_TYPE_UINT16, L1s2, (uint64_t)N,
+                   (uint64_t)gq.rank2, (uint64_t)N * 2, 64u, (uint32_t)(gq.rank2 / 2),
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return SVDQ_ERR_CUDA;
+  } else {
+    std::memset(&maps.l1s2, 0, sizeof(maps.l1s2));
+  }
   // test hook: the kernel's loader issues nothing, so that its pipeline waits
   // time out after 100 ms (status SVDQ_DEV_TIMEOUT)
   const int test_stall = g_gemm_stall.load(std::memory_order_relaxed) ? 1 : 0;
   cudaError_t e = svdq::launch_gemm_w4a4(maps, block_n, a_scales, w_scales, w_tensor_scale,
-                                         bias, Y, M, N, K, rank, epi, qe, dev_status,
+                                         bias, Y, M, N, K, rank, epi, qe, gq, dev_status,
                                          test_stall, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
@@ -237,8 +261,8 @@ svdq_status svdq_gemm_w4a4(const uint8_t* a_codes, const uint8_t* a_scales,
                            const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
                            int* dev_status, void* stream) {
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, Y,
-                   M, N, K, rank, svdq::GemmEpilogue::kPlain, svdq::QkvEpilogue{}, dev_status,
-                   stream);
+                   M, N, K, rank, svdq::GemmEpilogue::kPlain, svdq::QkvEpilogue{},
+                   svdq::GeluQuantEpilogue{}, nullptr, dev_status, stream);
 }
 
 svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
@@ -247,8 +271,8 @@ svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
                                 const uint16_t* L2s, const uint16_t* bias, uint16_t* H, int M,
                                 int N, int K, int rank, int* dev_status, void* stream) {
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, H,
-                   M, N, K, rank, svdq::GemmEpilogue::kGelu, svdq::QkvEpilogue{}, dev_status,
-                   stream);
+                   M, N, K, rank, svdq::GemmEpilogue::kGelu, svdq::QkvEpilogue{},
+                   svdq::GeluQuantEpilogue{}, nullptr, dev_status, stream);
 }
 
 svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,
@@ -261,7 +285,24 @@ svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,
                                void* stream) {
   const svdq::QkvEpilogue qe{norm_q, norm_k, rope_cos, rope_sin, eps, N / 3};
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias,
-                   QKV, M, N, K, rank, svdq::GemmEpilogue::kQkv, qe, dev_status, stream);
+                   QKV, M, N, K, rank, svdq::GemmEpilogue::kQkv, qe,
+                   svdq::GeluQuantEpilogue{}, nullptr, dev_status, stream);
+}
+
+svdq_status svdq_gemm_w4a4_gelu_quant(const uint8_t* a_codes, const uint8_t* a_scales,
+                                      const uint8_t* w_codes, const uint8_t* w_scales,
+                                      float w_tensor_scale, const uint16_t* lora_act,
+                                      const uint16_t* L2s, const uint16_t* bias,
+                                      const float* inv_lambda2, const uint16_t* L1s2,
+                                      int rank2, uint8_t* a2_codes, uint8_t* a2_scales,
+                                      uint16_t* lora_act2, uint16_t* H, float* scratch,
+                                      size_t scratch_bytes, int M, int N, int K, int rank,
+                                      int* dev_status, void* stream) {
+  const svdq::GeluQuantEpilogue gq{inv_lambda2, a2_codes, a2_scales, scratch,  H,
+                                   lora_act2,   rank2,    scratch_bytes};
+  return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, H,
+                   M, N, K, rank, svdq::GemmEpilogue::kGeluQuant, svdq::QkvEpilogue{}, gq, L1s2,
+                   dev_status, stream);
 }
 
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

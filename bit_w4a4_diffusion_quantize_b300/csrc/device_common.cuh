@@ -175,6 +175,18 @@ SVDQ_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 #endif
   return ok != 0;
 }
+// Non-blocking test of an mbarrier phase (never suspends).
+SVDQ_DEVINL bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on an mbarrier phase.  Returns false (and reports) on timeout.
 SVDQ_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                            uint64_t timeout_ns = kWaitTimeoutNs) {

@@ -81,6 +81,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "act_quant.cuh"
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -96,17 +97,22 @@ constexpr int SF_WARP0 = 2;   // warps 2..5
 constexpr int EPI_WARP0 = 6;  // warps 6..21
 constexpr int EPI_WARPS = 16;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int SMEM_BUDGET = 224 * 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;  // dynamic shared memory of one CTA
 constexpr int kMaxDevices = 64;
+// GELU + quantization: at most this many CTA pairs (the scratch holds
+// kGqMaxPairs + ceil(M / 256) slots of segment sums)
+constexpr int kGqMaxPairs = 128;
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 // epilogue kinds: bf16 Y; bf16 gelu_tanh(Y); Y with its Q and K heads
 // RMS-normalized and rotated (fused QKV projection)
-constexpr int kEpiPlain = 0, kEpiGelu = 1, kEpiQkv = 2;
+constexpr int kEpiPlain = 0, kEpiGelu = 1, kEpiQkv = 2, kEpiGeluQuant = 3;
 constexpr int kHeadDim = 128;  // QKV epilogue: channels of one head
 
-template <int BN, int RANK, int EPI>
+// RANK2: rank of the next layer's down projection (GELU + quantization
+// epilogue only; 0 for the others)
+template <int BN, int RANK, int EPI, int RANK2 = 0>
 struct Cfg {
   static constexpr int BH = BN / 2;  // W rows held by one CTA of the pair
   static constexpr int A_BYTES = BM * BK_BYTES;
@@ -119,7 +125,6 @@ struct Cfg {
   static constexpr int LB_BYTES = BH * LROW;
   static_assert(LA_BYTES <= A_BYTES && LB_BYTES <= B_BYTES, "rank-r operands fit a ring slot");
   static constexpr int BIAS_BYTES = BN * 2;
-  static constexpr int MISC_BYTES = 512;
   // QKV: per-lane partial sums of squares exchanged by the two warps of a head
   // (two buffers), and one barrier per warp pair
   static constexpr int XSUM_BYTES = EPI == kEpiQkv ? 2 * 16 * 32 * 4 : 0;
@@ -133,31 +138,60 @@ struct Cfg {
   static constexpr int OUT_ROW_BYTES = EPI_COLS * 2;                 // 128 or 64
   static constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
   static constexpr int OUT_BYTES = TMA_OUT ? EPI_WARPS * OUT_WARP_BYTES : 0;
-  static constexpr int FIXED_BYTES = OUT_BYTES + 2 * BIAS_BYTES + XSUM_BYTES + MISC_BYTES;
+  // GELU + quantization: per tile this CTA's half of the next layer's L1s
+  // slice (rank2/2 rows x BN columns, [BN/64 chunks][rows][64], 128B swizzle:
+  // the B operand of the down-projection MMAs, whose A operand is the staged H
+  // tile) and the e4m3 reciprocal table of the quantization.  The per-tile
+  // slices (bias, L1s) are single-buffered there, so that four ring stages fit.
+  static constexpr bool GQ = EPI == kEpiGeluQuant;
+  static constexpr int R2H = RANK2 / 2;
+  static constexpr int L1S2_BYTES = GQ ? (BN / 64) * R2H * 128 : 0;
+  static constexpr int TAB_BYTES = GQ ? 128 * 8 : 0;
+  static constexpr int EBUF = GQ ? 1 : 2;  // buffers of the per-tile epilogue slices
+  static constexpr int FIXED_BYTES =
+      OUT_BYTES + L1S2_BYTES + TAB_BYTES + EBUF * BIAS_BYTES + XSUM_BYTES;
+  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full,
+  // acc_empty, mma_done, pair[PAIR_BARS], and for GELU + quantization h_ready,
+  // l2q_full, l2q_empty, l1s2_empty
+  static constexpr int GQ_BARS = GQ ? 4 : 0;
+  static constexpr int BAR_BYTES_MAX = (3 * 6 + 5 + PAIR_BARS + GQ_BARS) * 8;
   // TMEM columns: accumulator [0, BN), then per stage the scales of A and B
   static constexpr int SF_COLS_A = 4 * KB_PER_TILE;
   static constexpr int SF_COLS_B = 4 * KB_PER_TILE * (BN / 128);
   static constexpr int SF_STAGE_COLS = SF_COLS_A + SF_COLS_B;
   static constexpr int SF_BASE = BN;
+  // ring depth: what shared memory (less the fixed areas, the barriers, 16
+  // bytes of flags and 1024 bytes of base-alignment slack) and TMEM hold
   static constexpr int STAGES =
-      cmin(cmin(6, (SMEM_BUDGET - 1024 - FIXED_BYTES) / STAGE_BYTES),
-           ((int)TMEM_COLS - SF_BASE) / SF_STAGE_COLS);
+      cmin(cmin(6, (SMEM_LIMIT - 1024 - 16 - BAR_BYTES_MAX - FIXED_BYTES) / STAGE_BYTES),
+           ((int)TMEM_COLS - SF_BASE - RANK2) / SF_STAGE_COLS);
+  // GELU + quantization: the down-projection accumulator after the scales
+  static constexpr int L2Q_COL = SF_BASE + STAGES * SF_STAGE_COLS;
   static constexpr int OFF_A = 0;  // slot areas 1024-aligned (swizzle atoms)
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 1024-aligned
-  static constexpr int OFF_BIAS = OFF_OUT + OUT_BYTES;
-  static constexpr int OFF_XSUM = OFF_BIAS + 2 * BIAS_BYTES;
+  static constexpr int OFF_L1S2 = OFF_OUT + OUT_BYTES;  // 1024-aligned
+  static constexpr int OFF_TAB = OFF_L1S2 + L1S2_BYTES;
+  static constexpr int OFF_BIAS = OFF_TAB + TAB_BYTES;
+  static constexpr int OFF_XSUM = OFF_BIAS + EBUF * BIAS_BYTES;
   static constexpr int OFF_BAR = OFF_XSUM + XSUM_BYTES;
-  // barriers: full[S], empty[S], sf_full[S], bias_empty[2], acc_full,
-  // acc_empty, mma_done, pair[PAIR_BARS]
-  static constexpr int NUM_BARS = 3 * STAGES + 5 + PAIR_BARS;
+  static constexpr int NUM_BARS = 3 * STAGES + 5 + PAIR_BARS + GQ_BARS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + base alignment slack
   static_assert(STAGES >= 2, "pipeline depth");
-  static_assert(SF_BASE + STAGES * SF_STAGE_COLS <= (int)TMEM_COLS, "TMEM budget");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SF_BASE + STAGES * SF_STAGE_COLS + RANK2 <= (int)TMEM_COLS, "TMEM budget");
+  static_assert(!GQ || (BN == 256 && (RANK2 == 32 || RANK2 == 64)),
+                "GELU + quantization: 256-column tiles, next-layer rank 32 or 64");
+  static_assert(OFF_L1S2 % 1024 == 0 && (L1S2_BYTES / (BN / 64 > 0 ? BN / 64 : 1)) % 1024 == 0,
+                "L1s2 chunks keep the swizzle atoms aligned");
+  // the down-projection MMAs of the next layer: kind::f16 bf16, M = 256 over
+  // the pair, N = RANK2
+  static constexpr uint32_t IDESC_L2Q = (1u << 4) | (1u << 7) | (1u << 10) |
+                                        ((uint32_t)(RANK2 >> 3) << 17) |
+                                        ((uint32_t)((2 * BM) >> 4) << 24);
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
   static_assert(B_BYTES % 1024 == 0, "W half tiles keep the 1024-byte swizzle atoms aligned");
   static constexpr SmemLayout LSW =
       LROW == 128 ? kSwizzle128B : (LROW == 64 ? kSwizzle64B : kSwizzle32B);
@@ -304,17 +338,20 @@ SVDQ_DEVINL void transpose_chunks(uint32_t (&c)[4 * CH], int lane) {
   }
 }
 
-template <int BN, int RANK, int EPI>
+template <int BN, int RANK, int EPI, int RANK2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm_w4a4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                 const __grid_constant__ CUtensorMap tm_lora,
                 const __grid_constant__ CUtensorMap tm_l2s,
-                const __grid_constant__ CUtensorMap tm_y, const uint8_t* __restrict__ a_scales,
+                const __grid_constant__ CUtensorMap tm_y,
+                const __grid_constant__ CUtensorMap tm_l1s2, const uint8_t* __restrict__ a_scales,
                 const uint8_t* __restrict__ w_scales, float s_T,
                 const uint16_t* __restrict__ bias, uint16_t* __restrict__ Y, int M, int N, int K,
-                const QkvEpilogue qe, int* dev_status, int test_stall, uint64_t wait_ns) {
+                const QkvEpilogue qe, const GeluQuantEpilogue gq, int* dev_status, int test_stall,
+                uint64_t wait_ns) {
   static_assert(EPI != kEpiQkv || BN == 2 * kHeadDim, "QKV epilogue: two heads per tile");
-  using C = Cfg<BN, RANK, EPI>;
+  using C = Cfg<BN, RANK, EPI, RANK2>;
+  constexpr bool GQ = C::GQ;
   constexpr int STAGES = C::STAGES;
   SVDQ_TR_SETUP;
   extern __shared__ uint8_t smem_raw[];
@@ -328,6 +365,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + 1;       // used in the even CTA
   uint64_t* mma_done = acc_empty + 1;       // used in the even CTA
   uint64_t* pair_bar = mma_done + 1;        // [PAIR_BARS]
+  // GELU + quantization: H staged (even CTA; both CTAs' epilogue warps), the
+  // next layer's down projection of a tile done (both CTAs), its accumulator
+  // read at the end of a segment (even CTA; the 4 reading warps of both CTAs),
+  // the L1s2 buffer free (both CTAs)
+  uint64_t* h_ready = pair_bar + C::PAIR_BARS;
+  uint64_t* l2q_full = h_ready + 1;
+  uint64_t* l2q_empty = l2q_full + 1;
+  uint64_t* l1s2_empty = l2q_empty + 1;
+  constexpr int EBUF = C::EBUF;  // bias slice buffers
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
   volatile uint32_t* abort_flag = &misc[1];
 
@@ -339,14 +385,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int m_tiles = (M + BM - 1) / BM;
   const int num_ptiles = ((m_tiles + 1) / 2) * n_tiles;  // 256-row pair tiles
   const int pair = (int)blockIdx.x >> 1, n_pairs = (int)gridDim.x >> 1;
-  const int my_tiles = pair < num_ptiles ? (num_ptiles - 1 - pair) / n_pairs + 1 : 0;
+  // Pair tiles pt (m pair pt / n_tiles, n tile pt % n_tiles) are dealt out
+  // round robin; with GELU + quantization each pair takes one contiguous range
+  // of them instead, [pt_begin, pt_begin + my_tiles), so that the next
+  // layer's down projection accumulates in TMEM over the n tiles of one m
+  // pair (a segment) and is written out once per segment.
+  int pt_begin = pair, my_tiles = 0;
+  if constexpr (GQ) {
+    pt_begin = (int)((long long)pair * num_ptiles / n_pairs);
+    my_tiles = (int)((long long)(pair + 1) * num_ptiles / n_pairs) - pt_begin;
+  } else {
+    my_tiles = pair < num_ptiles ? (num_ptiles - 1 - pair) / n_pairs + 1 : 0;
+  }
+  auto tile_pt = [&](int j) { return GQ ? pt_begin + j : pair + j * n_pairs; };
   // tile j of this CTA: m tile 2 * (pt / n_tiles) + crank (may lie past M when
   // m_tiles is odd: it is computed on zero-filled rows and not stored)
   auto tile_mn = [&](int j, int& m_tile, int& n_tile) {
-    const int pt = pair + j * n_pairs;
+    const int pt = tile_pt(j);
     m_tile = 2 * (pt / n_tiles) + (int)crank;
     n_tile = pt % n_tiles;
   };
+  // GELU + quantization: first / last tile of a segment
+  auto seg_first = [&](int j) { return j == 0 || tile_pt(j) % n_tiles == 0; };
+  auto seg_last = [&](int j) { return j == my_tiles - 1 || (tile_pt(j) + 1) % n_tiles == 0; };
   // the even CTA's copy of a barrier, as a shared::cluster address
   auto at_even = [](uint64_t* bar) { return cluster_map(smem_u32(bar), 0u); };
   // stop this CTA and tell the peer to stop too (its waits would otherwise
@@ -365,19 +426,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&empty[s], 1);     // the even CTA's MMA commit
       mbar_init(&sf_full[s], 8);   // the 4 scale warps of each CTA of the pair
     }
-    mbar_init(&bias_empty[0], EPI_WARPS);
-    mbar_init(&bias_empty[1], EPI_WARPS);
+    for (int b = 0; b < EBUF; ++b) mbar_init(&bias_empty[b], EPI_WARPS);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * EPI_WARPS);  // the epilogue warps of both CTAs
     mbar_init(mma_done, 1);
     for (int b = 0; b < C::PAIR_BARS; ++b) mbar_init(&pair_bar[b], 2);
+    if (GQ) {
+      mbar_init(h_ready, 2 * EPI_WARPS);
+      mbar_init(l2q_full, 1);
+      mbar_init(l2q_empty, 8);  // warps 0-3 of the epilogue, both CTAs
+      mbar_init(l1s2_empty, 1);
+    }
     misc[1] = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     prefetch_tmap(&tm_lora);
     prefetch_tmap(&tm_l2s);
-    if (C::TMA_OUT) prefetch_tmap(&tm_y);
+    if (C::TMA_OUT && (!GQ || gq.h_out)) prefetch_tmap(&tm_y);  // (no H: an unused map)
+    if (GQ) prefetch_tmap(&tm_l1s2);
+  }
+  if (GQ && threadIdx.x < 128) {
+    // two-term reciprocals of the 127 positive e4m3 values (code 0: zeros)
+    const float2 v = threadIdx.x == 0 || threadIdx.x == 127 ? make_float2(0.0f, 0.0f)
+                                                            : recip2(e4m3_to_f32(threadIdx.x));
+    *reinterpret_cast<float2*>(smem + C::OFF_TAB + 8 * threadIdx.x) = v;
   }
   // both CTAs resident and their barriers initialised before the collective
   // TMEM allocation and before any arrival from the peer
@@ -413,18 +486,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (kt == k_tiles) {
             // rank-r operands of tile j (own rows, own half of L2s) and its
             // bias slice (all BN columns: this CTA stores every column)
-            if (bias && !mbar_wait(&bias_empty[j & 1], (uint32_t)((j >> 1) & 1) ^ 1u,
+            // (GELU + quantization: also this CTA's half of the next layer's
+            // L1s slice)
+            if (bias && !mbar_wait(&bias_empty[j % EBUF], (uint32_t)((j / EBUF) & 1) ^ 1u,
                                    dev_status, wait_ns)) {
               abort_pair();
               break;
             }
+            // (GELU + quantization: the previous tile's down projection has
+            // read the L1s2 buffer)
+            if (GQ && !mbar_wait(l1s2_empty, (uint32_t)(j & 1) ^ 1u, dev_status, wait_ns)) {
+              abort_pair();
+              break;
+            }
             mbar_arrive_expect_tx(&full[s], (uint32_t)(C::LA_BYTES + C::LB_BYTES +
-                                                       (bias ? C::BIAS_BYTES : 0)));
+                                                       (bias ? C::BIAS_BYTES : 0) +
+                                                       C::L1S2_BYTES));
             tma_load_2d(sa, &tm_lora, &full[s], 0, m0);
             tma_load_2d(sb, &tm_l2s, &full[s], 0, nh);
             if (bias)
-              bulk_load(smem + C::OFF_BIAS + (j & 1) * C::BIAS_BYTES, bias + n0,
+              bulk_load(smem + C::OFF_BIAS + (j % EBUF) * C::BIAS_BYTES, bias + n0,
                         (uint32_t)C::BIAS_BYTES, &full[s]);
+            if (GQ) {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(smem + C::OFF_L1S2 + c * (C::R2H * 128), &tm_l1s2, &full[s],
+                            n0 + 64 * c, (int)crank * C::R2H);
+            }
             SVDQ_TR(424, 8, j);
           } else {
             const int nkb = min(KB_PER_TILE, kb_total - kt * KB_PER_TILE);
@@ -466,17 +554,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool tail_half = (kb_total % KB_PER_TILE) != 0;  // last k tile has 2 MMA steps
       int s = 0;
       uint32_t ph = 0;  // ring position: slot and phase parity
-      // Position (s, ph) is ready when the scale warps of both CTAs have seen
-      // their slot land and put its scales in their TMEM (sf_full: the scale
-      // warps waited on this CTA's `full` first, so it orders the TMA data too).
-      auto ready = [&](int s_, uint32_t ph_) -> bool {
-        const bool ok = mbar_wait(&sf_full[s_], ph_, dev_status, wait_ns);
-        tc_fence_after();
-        return __all_sync(0xFFFFFFFFu, ok);
-      };
       // frees slot s in both CTAs once the MMAs issued so far have read it
       auto release_slot = [&](int s_) {
         tc_commit_pair_warp2(empty_c0 + 8u * (uint32_t)s_, empty_c1 + 8u * (uint32_t)s_);
+      };
+      // GELU + quantization: the next layer's down projection of tile t, its
+      // staged H (both CTAs' 128 rows, [BN/64 chunks][128 rows][64]) times the
+      // L1s2 slice, accumulated over the segment into the RANK2 TMEM columns at
+      // L2Q_COL.  It is issued between the k tiles of the following tile, once
+      // H is staged (h_ready) and, at a segment's first tile, the previous
+      // segment's sums were read (l2q_empty, one phase per segment).
+      int l2q_pending = -1, l2q_segs = 0;
+      auto l2q_issue = [&](int t) {
+        tc_fence_after();
+        const uint32_t hb = smem_u32(smem + C::OFF_OUT);
+        const uint32_t lb = smem_u32(smem + C::OFF_L1S2);
+        const uint32_t acc0 = seg_first(t) ? 0u : 1u;
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16_pair_warp(
+                tmem + (uint32_t)C::L2Q_COL,
+                smem_desc(hb + c * (4 * C::OUT_WARP_BYTES) + kk * 32, 16, 1024, kSwizzle128B),
+                smem_desc(lb + c * (C::R2H * 128) + kk * 32, 16, 1024, kSwizzle128B),
+                C::IDESC_L2Q, (c | kk) != 0 ? 1u : acc0);
+        tc_commit_pair_warp2(cluster_map(smem_u32(l2q_full), 0u),
+                             cluster_map(smem_u32(l2q_full), 1u));
+        tc_commit_pair_warp2(cluster_map(smem_u32(l1s2_empty), 0u),
+                             cluster_map(smem_u32(l1s2_empty), 1u));
+        if (seg_first(t)) ++l2q_segs;
+      };
+      // the accumulator of the previous segment has been read (or there is none)
+      auto l2q_free = [&](int t, bool block) -> bool {
+        if (!seg_first(t)) return true;
+        const uint32_t par = (uint32_t)(l2q_segs & 1) ^ 1u;
+        return block ? mbar_wait(l2q_empty, par, dev_status, wait_ns) : mbar_test(l2q_empty, par);
+      };
+      auto l2q_try = [&]() {  // non-blocking
+        if (!GQ || l2q_pending < 0) return;
+        const int t = l2q_pending;
+        const bool r = mbar_test(h_ready, (uint32_t)(t & 1)) && l2q_free(t, false);
+        if (__all_sync(0xFFFFFFFFu, r)) {
+          l2q_issue(t);
+          l2q_pending = -1;
+        }
+      };
+      auto l2q_finish = [&]() -> bool {  // blocking
+        if (!GQ || l2q_pending < 0) return true;
+        const int t = l2q_pending;
+        const bool r = mbar_wait(h_ready, (uint32_t)(t & 1), dev_status, wait_ns) &&
+                       l2q_free(t, true);
+        if (!__all_sync(0xFFFFFFFFu, r)) return false;
+        l2q_issue(t);
+        l2q_pending = -1;
+        return true;
+      };
+      // Position (s, ph) is ready when the scale warps of both CTAs have seen
+      // their slot land and put its scales in their TMEM (sf_full: the scale
+      // warps waited on this CTA's `full` first, so it orders the TMA data too).
+      // With GELU + quantization a rank-r slot can wait, through the L1s2
+      // buffer, for the previous tile's down projection: while one is
+      // pending, the wait keeps trying to issue it.
+      auto ready = [&](int s_, uint32_t ph_) -> bool {
+        bool ok;
+        if (GQ && l2q_pending >= 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (true) {
+            if (__all_sync(0xFFFFFFFFu, mbar_test(&sf_full[s_], ph_))) {
+              ok = true;
+              break;
+            }
+            l2q_try();
+            if (globaltimer_ns() - t0 > wait_ns) {
+              report_timeout(dev_status);
+              ok = false;
+              break;
+            }
+          }
+        } else {
+          ok = mbar_wait(&sf_full[s_], ph_, dev_status, wait_ns);
+        }
+        tc_fence_after();
+        return __all_sync(0xFFFFFFFFu, ok);
       };
       for (int j = 0; j < my_tiles && !__any_sync(0xFFFFFFFFu, *abort_flag != 0); ++j) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_empty, (uint32_t)(j & 1) ^ 1u, dev_status,
@@ -511,6 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // first MMA, the wait for the next position after its second
           mma(0, kt != 0 ? 1u : 0u);
           if (prev >= 0) release_slot(prev);
+          l2q_try();
           if (tail_half && kt + 1 == k_tiles) {
             ok = ready(sn, phn);
             mma(1, 1u);
@@ -561,10 +722,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_commit_pair_warp2(cluster_map(smem_u32(acc_full), 0u),
                              cluster_map(smem_u32(acc_full), 1u));
         if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+        if (GQ) {
+          if (!l2q_finish()) {  // the previous tile's, if the k tiles did not fit it in
+            abort_pair();
+            break;
+          }
+          l2q_pending = j;
+        }
       }
+      if (GQ && !__any_sync(0xFFFFFFFFu, *abort_flag != 0) && !l2q_finish()) abort_pair();
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) {  // wake both epilogues after an abort
         tc_commit_pair_warp2(cluster_map(smem_u32(acc_full), 0u),
                              cluster_map(smem_u32(acc_full), 1u));
+        if (GQ)
+          tc_commit_pair_warp2(cluster_map(smem_u32(l2q_full), 0u),
+                               cluster_map(smem_u32(l2q_full), 1u));
       }
       // no MMA may still write either TMEM when the pair frees it
       tc_commit_pair_warp(cluster_map(smem_u32(mma_done), 0u));
@@ -661,19 +833,119 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // the bias slice landed with this tile's rank-r slot (the rank-r MMAs
       // waited for it, through sf_full, before acc_full was signalled)
       const uint16_t* bsm =
-          bias ? reinterpret_cast<const uint16_t*>(smem + C::OFF_BIAS + (j & 1) * C::BIAS_BYTES)
+          bias ? reinterpret_cast<const uint16_t*>(smem + C::OFF_BIAS + (j % EBUF) * C::BIAS_BYTES)
                : nullptr;
       // bf16 pairs in place: pair i lands in v[i] (read from v[2i], v[2i+1])
 #pragma unroll
       for (int c = 0; c < C::EPI_COLS / 32; ++c)
-        pack_cols32<EPI == kEpiGelu>(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr,
-                                     &v[16 * c]);
+        pack_cols32<EPI == kEpiGelu || GQ>(&v[32 * c], s_T, bsm ? bsm + col0 + 32 * c : nullptr,
+                                           &v[16 * c]);
       uint32_t(&pk)[4 * CH] = *reinterpret_cast<uint32_t(*)[4 * CH]>(&v[0]);
       if (bsm) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bias_empty[j & 1]);
+        if (lane == 0) mbar_arrive(&bias_empty[j % EBUF]);
       }
-      if constexpr (C::TMA_OUT) {
+      if constexpr (GQ) {
+        // H = bf16(gelu(Y)) of this lane's row: staged for the down-projection
+        // MMAs (and the optional store of H), then quantized as the next
+        // layer's input, 4 blocks of 16 columns
+        constexpr int swz_mask = 7;  // 128-byte rows, 128B swizzle
+        const int row = m0 + 32 * q + lane;
+        // the down-projection MMAs read 64-column chunk c as 128 rows in
+        // order: lane quarter q of the chunk's warps stages at block 4c + q
+        uint8_t* gstage = smem + C::OFF_OUT + ((e >> 2) * 4 + q) * C::OUT_WARP_BYTES;
+        // the staging area is free: the previous tile's down projection has
+        // read it (l2q_full), and its store of H has left it
+        if (j > 0) {
+          const bool got =
+              mbar_wait(l2q_full, (uint32_t)((j - 1) & 1), dev_status, wait_ns) && !*abort_flag;
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            abort_pair();
+            break;
+          }
+        }
+        if (gq.h_out && lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int o = lane * C::OUT_ROW_BYTES + 16 * c;
+          sts128(gstage + (o ^ (((o >> 7) & swz_mask) << 4)), pk[4 * c], pk[4 * c + 1],
+                 pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();  // generic writes, before the MMAs (async proxy) read them
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(at_even(h_ready));
+          if (gq.h_out && m0 + 32 * q < M) {
+            tma_store_2d(&tm_y, gstage, n0 + col0, m0 + 32 * q);
+            bulk_commit_group();
+          }
+        }
+        // the next layer's activation quantization of the row's 64 columns
+        const float2* tabp = reinterpret_cast<const float2*>(smem + C::OFF_TAB);
+        const float2 r6 = recip2(6.0f);
+        // inv_lambda of the columns: the same 64 floats for every lane (one
+        // broadcast load each, from L1 after the first warp)
+        const float4* invg = reinterpret_cast<const float4*>(gq.inv_lambda2 + n0 + col0);
+        uint2 cw[4];
+        uint32_t sw = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = pk[8 * b + i];
+          float inv[16];
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 iv = __ldg(invg + 4 * b + i4);
+            inv[4 * i4] = iv.x;
+            inv[4 * i4 + 1] = iv.y;
+            inv[4 * i4 + 2] = iv.z;
+            inv[4 * i4 + 3] = iv.w;
+          }
+          uint32_t sb;
+          quant_block16(w, inv, r6, tabp, cw[b], sb);
+          sw |= sb << (8 * b);
+        }
+        if (row < M) {
+          uint4* cp = reinterpret_cast<uint4*>(gq.a2_codes + (size_t)row * (N / 2) + (n0 + col0) / 2);
+          cp[0] = make_uint4(cw[0].x, cw[0].y, cw[1].x, cw[1].y);
+          cp[1] = make_uint4(cw[2].x, cw[2].y, cw[3].x, cw[3].y);
+          *reinterpret_cast<uint32_t*>(gq.a2_scales +
+                                       ((size_t)(row >> 7) * (N / 64) + (n0 + col0) / 64) * 512 +
+                                       (row & 31) * 16 + ((row >> 5) & 3) * 4) = sw;
+        }
+        // at the segment's last tile, warps 0-3 (one per lane quarter): the
+        // segment's down-projection sums of their 32 rows, to scratch slot
+        // pair + m pair (256 rows x RANK2 floats; unique: a later pair covers
+        // no earlier m pair)
+        if (e < 4 && seg_last(j)) {
+          const bool got =
+              mbar_wait(l2q_full, (uint32_t)(j & 1), dev_status, wait_ns) && !*abort_flag;
+          if (!__all_sync(0xFFFFFFFFu, got)) {
+            abort_pair();
+            break;
+          }
+          tc_fence_after();
+          uint32_t pv[RANK2];
+#pragma unroll
+          for (int c = 0; c < RANK2 / 32; ++c)
+            tmem_ld_32x32b_x32(lane_base + (uint32_t)(C::L2Q_COL + 32 * c),
+                               *reinterpret_cast<uint32_t(*)[32]>(&pv[32 * c]));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(at_even(l2q_empty));
+          if (row < M) {
+            const size_t slot = (size_t)(pair + tile_pt(j) / n_tiles);
+            uint4* pp = reinterpret_cast<uint4*>(
+                gq.partial + (slot * (2 * BM) + (size_t)crank * BM + 32 * q + lane) * RANK2);
+#pragma unroll
+            for (int i = 0; i < RANK2 / 4; ++i)
+              pp[i] = make_uint4(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
+          }
+        }
+      } else if constexpr (C::TMA_OUT) {
         // rows at or past M are clipped by the tensor map (a block wholly past
         // M is not stored at all)
         constexpr int swz_mask = C::OUT_ROW_BYTES == 128 ? 7 : 3;  // 128B / 64B swizzle
@@ -742,6 +1014,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // every TMA store of this warp has completed (and left its staging area)
     if (C::TMA_OUT && lane == 0) bulk_wait_group0();
+    // GELU + quantization: the last tile's down projection has read the
+    // staging area before the CTA may leave (the even CTA's MMAs read both)
+    if (GQ && my_tiles > 0 && !*abort_flag)
+      mbar_wait(l2q_full, (uint32_t)((my_tiles - 1) & 1), dev_status, wait_ns);
   }
 
   tc_fence_before();
@@ -760,13 +1036,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, int RANK, int EPI>
+// GELU + quantization, second kernel: lora2[m][i] = bf16( the sum, over the
+// CTA pairs p that covered m pair mp = m / 256 in ascending order, of
+// partial[p + mp][m % 256][i] ).  The pairs' tile ranges are those of the
+// GEMM: pair p took pair tiles [p T / P, (p + 1) T / P) (T P < 2^31, checked
+// by the caller).  One thread per 4 consecutive outputs of a row.
+__device__ __forceinline__ int gq_owner(int t, int num_ptiles, int n_pairs) {
+  return (int)(((unsigned)(t + 1) * (unsigned)n_pairs - 1u) / (unsigned)num_ptiles);
+}
+__global__ void __launch_bounds__(256)
+    k_lora_reduce(const float* __restrict__ partial, int M, int rank2, int num_ptiles,
+                  int n_pairs, int n_tiles, uint16_t* __restrict__ lora2) {
+  grid_dep_launch();
+  grid_dep_wait();  // the GEMM's segment sums are complete
+  const int quads = rank2 >> 2;
+  const int total = M * quads;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int m = idx / quads, i4 = idx - m * quads, mp = m >> 8;
+    const int p_lo = gq_owner(mp * n_tiles, num_ptiles, n_pairs);
+    const int p_hi = gq_owner(mp * n_tiles + n_tiles - 1, num_ptiles, n_pairs);
+    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int p = p_lo; p <= p_hi; ++p) {
+      // (a pair without tiles wrote nothing)
+      if ((unsigned)(p + 1) * (unsigned)num_ptiles / (unsigned)n_pairs ==
+          (unsigned)p * (unsigned)num_ptiles / (unsigned)n_pairs)
+        continue;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(
+                                 partial + (((size_t)(p + mp) << 8) + (m & 255)) * rank2) +
+                             i4);
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    *reinterpret_cast<uint2*>(lora2 + (size_t)m * rank2 + 4 * i4) =
+        make_uint2((uint32_t)f32_to_bf16_rn(sum.x) | ((uint32_t)f32_to_bf16_rn(sum.y) << 16),
+                   (uint32_t)f32_to_bf16_rn(sum.z) | ((uint32_t)f32_to_bf16_rn(sum.w) << 16));
+  }
+}
+
+template <int BN, int RANK, int EPI, int RANK2 = 0>
 cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
                      float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
-                     const QkvEpilogue& qe, int* dev_status, int test_stall, int num_sms,
-                     cudaStream_t stream) {
-  using C = Cfg<BN, RANK, EPI>;
-  auto kern = k_gemm_w4a4<BN, RANK, EPI>;
+                     const QkvEpilogue& qe, const GeluQuantEpilogue& gq, int* dev_status,
+                     int test_stall, int num_sms, cudaStream_t stream) {
+  using C = Cfg<BN, RANK, EPI, RANK2>;
+  auto kern = k_gemm_w4a4<BN, RANK, EPI, RANK2>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -804,15 +1120,28 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
     max_pairs_of[dev].store(n, std::memory_order_relaxed);
   }
   const int m_tiles = (M + BM - 1) / BM;
-  const int pairs_needed = ((m_tiles + 1) / 2) * (N / BN);
-  const int pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
+  const int num_ptiles = ((m_tiles + 1) / 2) * (N / BN);
+  int pairs = num_ptiles < max_pairs ? num_ptiles : max_pairs;
+  if (EPI == kEpiGeluQuant && pairs > kGqMaxPairs) pairs = kGqMaxPairs;  // scratch slots
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, maps.a_codes, maps.w_codes, maps.lora, maps.l2s, maps.y,
-                         a_scales,
-                         w_scales, s_T, bias, Y, M, N, K, qe, dev_status, test_stall,
-                         (uint64_t)(test_stall ? 100000000ull : kWaitTimeoutNs));
+                         maps.l1s2, a_scales, w_scales, s_T, bias, Y, M, N, K, qe, gq, dev_status,
+                         test_stall, (uint64_t)(test_stall ? 100000000ull : kWaitTimeoutNs));
   if (e != cudaSuccess) return e;
+  if (EPI == kEpiGeluQuant) {
+    cudaLaunchConfig_t rc = {};
+    const size_t total = (size_t)M * (gq.rank2 / 4);
+    const size_t blocks = (total + 255) / 256;
+    rc.gridDim = dim3((unsigned)(blocks < 4096 ? blocks : 4096), 1, 1);
+    rc.blockDim = dim3(256, 1, 1);
+    rc.stream = stream;
+    rc.attrs = &attr[1];  // programmatic dependent launch
+    rc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&rc, k_lora_reduce, (const float*)gq.partial, M, gq.rank2,
+                           num_ptiles, pairs, N / BN, gq.lora2);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -820,13 +1149,32 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
 template <int BN, int RANK>
 cudaError_t launch_qkv_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
                          float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
-                         const QkvEpilogue& qe, int* dev_status, int test_stall, int num_sms,
-                         cudaStream_t stream) {
+                         const QkvEpilogue& qe, const GeluQuantEpilogue& gq, int* dev_status,
+                         int test_stall, int num_sms, cudaStream_t stream) {
   if constexpr (BN == 2 * kHeadDim)
-    return launch_t<BN, RANK, kEpiQkv>(maps, a_scales, w_scales, s_T, bias, Y, M, N, K, qe,
+    return launch_t<BN, RANK, kEpiQkv>(maps, a_scales, w_scales, s_T, bias, Y, M, N, K, qe, gq,
                                        dev_status, test_stall, num_sms, stream);
   else
     return cudaErrorInvalidValue;
+}
+
+// the GELU + quantization epilogue exists for 256-column tiles only
+template <int BN, int RANK>
+cudaError_t launch_gq_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_t* w_scales,
+                        float s_T, const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                        const QkvEpilogue& qe, const GeluQuantEpilogue& gq, int* dev_status,
+                        int test_stall, int num_sms, cudaStream_t stream) {
+  if constexpr (BN == 256) {
+    if (gq.rank2 == 32)
+      return launch_t<BN, RANK, kEpiGeluQuant, 32>(maps, a_scales, w_scales, s_T, bias, Y, M, N,
+                                                   K, qe, gq, dev_status, test_stall, num_sms,
+                                                   stream);
+    if (gq.rank2 == 64)
+      return launch_t<BN, RANK, kEpiGeluQuant, 64>(maps, a_scales, w_scales, s_T, bias, Y, M, N,
+                                                   K, qe, gq, dev_status, test_stall, num_sms,
+                                                   stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -834,18 +1182,21 @@ cudaError_t launch_qkv_t(const GemmMaps& maps, const uint8_t* a_scales, const ui
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
                              uint16_t* Y, int M, int N, int K, int rank, GemmEpilogue epi,
-                             const QkvEpilogue& qe, int* dev_status, int test_stall,
-                             int num_sms, cudaStream_t stream) {
+                             const QkvEpilogue& qe, const GeluQuantEpilogue& gq,
+                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream) {
 #define SVDQ_GEMM_LAUNCH(BN_, R_, E_)                                                        \
   return launch_t<BN_, R_, E_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N, K,   \
-                               qe, dev_status, test_stall, num_sms, stream)
+                               qe, gq, dev_status, test_stall, num_sms, stream)
 #define SVDQ_GEMM_CASE(BN_, R_)                                                              \
   if (block_n == BN_ && rank == R_) {                                                        \
     if (epi == GemmEpilogue::kPlain) SVDQ_GEMM_LAUNCH(BN_, R_, kEpiPlain);                   \
     if (epi == GemmEpilogue::kGelu) SVDQ_GEMM_LAUNCH(BN_, R_, kEpiGelu);                     \
     if (epi == GemmEpilogue::kQkv)                                                           \
       return launch_qkv_t<BN_, R_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N,  \
-                                   K, qe, dev_status, test_stall, num_sms, stream);          \
+                                   K, qe, gq, dev_status, test_stall, num_sms, stream);      \
+    if (epi == GemmEpilogue::kGeluQuant)                                                     \
+      return launch_gq_t<BN_, R_>(maps, a_scales, w_scales, w_tensor_scale, bias, Y, M, N,   \
+                                  K, qe, gq, dev_status, test_stall, num_sms, stream);       \
   }
   SVDQ_GEMM_CASE(256, 16)
   SVDQ_GEMM_CASE(256, 32)

@@ -24,12 +24,30 @@ struct GemmMaps {
   CUtensorMap lora;     // lora_act [M][rank] bf16: box rank x 128 rows, swizzle = 2*rank bytes
   CUtensorMap l2s;      // L2s [N][rank] bf16: box rank x BN/2 rows, same swizzle
   CUtensorMap y;        // Y [M][N] bf16: box BN/4 x 32 rows, swizzle = BN/2 bytes (stores)
+  CUtensorMap l1s2;     // GELU + quantization only: the next layer's L1s [rank2][N] bf16,
+                        // box 64 x rank2/2 rows, 128B swizzle
 };
 
 // What svdq_gemm_w4a4's epilogue does after y = s_T * acc + bias is rounded to
 // bf16: nothing; GELU (tanh form); per-head RMS normalization and rotary
-// embedding of the Q and K column blocks (fused QKV projection, block_n 256).
-enum class GemmEpilogue { kPlain, kGelu, kQkv };
+// embedding of the Q and K column blocks (fused QKV projection, block_n 256);
+// GELU, then the next layer's activation quantization of the result (block_n
+// 256).
+enum class GemmEpilogue { kPlain, kGelu, kQkv, kGeluQuant };
+
+// Operands of the GELU + quantization epilogue (all null for the others): the
+// GELU output H [M][N] is quantized as the next linear's input X2 (K2 = N).
+struct GeluQuantEpilogue {
+  const float* inv_lambda2;  // [N] the next layer's smoothing
+  uint8_t* a2_codes;         // [M][N/2] e2m1 codes of H
+  uint8_t* a2_scales;        // scale tiles of H (rows M, K2 = N)
+  float* partial;            // scratch: [128 + ceil(M/256)][256][rank2] segment sums
+  uint16_t* h_out;           // [M][N] bf16 H, or null (H is not written)
+  uint16_t* lora2;           // [M][rank2] bf16 down projection (a second kernel adds the
+                             // segment sums)
+  int rank2;                 // 32 or 64
+  size_t scratch_bytes;      // bytes at `partial`
+};
 
 // Operands of the QKV epilogue (all null / zero for the others).
 struct QkvEpilogue {
@@ -44,8 +62,8 @@ struct QkvEpilogue {
 cudaError_t launch_gemm_w4a4(const GemmMaps& maps, int block_n, const uint8_t* a_scales,
                              const uint8_t* w_scales, float w_tensor_scale, const uint16_t* bias,
                              uint16_t* Y, int M, int N, int K, int rank, GemmEpilogue epi,
-                             const QkvEpilogue& qe, int* dev_status, int test_stall,
-                             int num_sms, cudaStream_t stream);
+                             const QkvEpilogue& qe, const GeluQuantEpilogue& gq,
+                             int* dev_status, int test_stall, int num_sms, cudaStream_t stream);
 
 // Largest K the AWQ GEMV stages in shared memory.
 int awq_max_k();

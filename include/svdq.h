@@ -103,6 +103,11 @@ typedef enum {
 /* byte sizes of the packed buffers */
 #define SVDQ_CODE_BYTES(rows, K) ((size_t)(rows) * (size_t)(K) / 2)
 #define SVDQ_SCALE_BYTES(rows, K) ((((size_t)(rows) + 127) / 128) * 128 * ((size_t)(K) / 16))
+/* device scratch of svdq_gemm_w4a4_gelu_quant: fp32 segment sums of the next
+ * layer's down projection, 128 + ceil(M/256) slots of 256 x rank2 (N is not
+ * used: every N takes the same) */
+#define SVDQ_GELU_QUANT_SCRATCH_BYTES(M, N, rank2) \
+  ((128 + ((size_t)(M) + 255) / 256) * 256 * (size_t)(rank2) * 4)
 
 /* Human-readable name of a status code (static string). */
 const char* svdq_status_string(svdq_status s);
@@ -231,6 +236,44 @@ svdq_status svdq_gemm_w4a4_gelu(const uint8_t* a_codes, const uint8_t* a_scales,
                                 const uint16_t* L2s, const uint16_t* bias, uint16_t* H,
                                 int M, int N, int K, int rank, int* dev_status,
                                 void* stream);
+
+/* svdq_gemm_w4a4_gelu for the first linear of an MLP whose output feeds the
+ * second SVDQ linear, with that second layer's activation side
+ * (svdq_quantize_act) fused into the epilogue as well (dothoosh.com, "How
+ * Nunchaku Lite halves the VRAM of diffusion models": the full engine's fused
+ * GELU/MLP kernels; the fused-kernel paragraph: the down projection runs with
+ * the quantization).  With H the bf16 GELU output svdq_gemm_w4a4_gelu returns
+ * for the same arguments, the outputs are exactly
+ *   a2_codes, a2_scales = those of svdq_quantize_act(H, inv_lambda2, K = N)
+ * (bit for bit), and
+ *   lora_act2[m][i] = bf16( sum_n H[m][n] L1s2[i][n] )
+ * accumulated in fp32 on the tensor cores.  The GEMM's persistent CTA pairs
+ * each take one contiguous range of 256 x 256 output tiles (m-pair-major); a
+ * pair accumulates the down projection in tensor memory over its tiles of one
+ * 256-row block and writes that fp32 segment sum to `scratch`; a second kernel
+ * adds the (at most a few) segment sums of each row in ascending pair order
+ * and rounds once.  H itself is written to `H` only when `H` is non-null.
+ * Inputs: as svdq_gemm_w4a4_gelu; inv_lambda2 [N] fp32 and L1s2 [rank2][N]
+ * bf16 of the second layer (svdq_pack_weights of that layer, K = N).
+ * Outputs: a2_codes SVDQ_CODE_BYTES(M, N), a2_scales SVDQ_SCALE_BYTES(M, N)
+ * (rows past M in the last 128-row tile are not written), lora_act2
+ * [M][rank2] bf16, H [M][N] bf16 (nullable).
+ * Scratch: `scratch` (device, caller-owned, contents on entry irrelevant, left
+ * holding the partial sums) of scratch_bytes >=
+ * SVDQ_GELU_QUANT_SCRATCH_BYTES(M, N, rank2) (SVDQ_ERR_SHAPE otherwise).
+ * Two kernels on `stream` (the second overlaps the first's tail through
+ * programmatic dependent launch).
+ * Sizes: N % 256 == 0, rank2 in {32, 64} (SVDQ_ERR_RANK otherwise); everything
+ * else as svdq_gemm_w4a4. */
+svdq_status svdq_gemm_w4a4_gelu_quant(const uint8_t* a_codes, const uint8_t* a_scales,
+                                      const uint8_t* w_codes, const uint8_t* w_scales,
+                                      float w_tensor_scale, const uint16_t* lora_act,
+                                      const uint16_t* L2s, const uint16_t* bias,
+                                      const float* inv_lambda2, const uint16_t* L1s2,
+                                      int rank2, uint8_t* a2_codes, uint8_t* a2_scales,
+                                      uint16_t* lora_act2, uint16_t* H, float* scratch,
+                                      size_t scratch_bytes, int M, int N, int K, int rank,
+                                      int* dev_status, void* stream);
 
 /* svdq_gemm_w4a4 for a fused Q|K|V projection, with the normalization of Q and
  * K and the rotary embedding in its epilogue (dothoosh.com, "How Nunchaku Lite

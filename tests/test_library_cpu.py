@@ -36,7 +36,7 @@ def _declared_functions():
 def test_library_exports_every_declared_symbol():
     names = _declared_functions()
     assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu",
-            "svdq_gemm_w4a4_qkv", "awq_gemv_w4a16",
+            "svdq_gemm_w4a4_qkv", "svdq_gemm_w4a4_gelu_quant", "awq_gemv_w4a16",
             "awq_pack_weights", "svdq_calib_absmax", "svdq_check_device",
             "svdq_status_string"} <= names
     raw = ctypes.CDLL(lib.LIB_PATH)
@@ -89,6 +89,16 @@ def _qkv(M=64, N=768, K=256, r=32, eps=1e-6, nq=ALIGNED, cos=ALIGNED):
                                             ALIGNED, M, N, K, r, None, None)
 
 
+def _gq(M=64, N=256, K=256, r=32, r2=32, scratch_bytes=None, H=None, inv2=ALIGNED,
+        scratch=ALIGNED, lora2=ALIGNED):
+    if scratch_bytes is None:
+        scratch_bytes = lib.gelu_quant_scratch_bytes(M, N, r2)
+    return lib.raw_lib().svdq_gemm_w4a4_gelu_quant(
+        ALIGNED, ALIGNED, ALIGNED, ALIGNED, ctypes.c_float(2.0 ** -10), ALIGNED, ALIGNED, None,
+        inv2, ALIGNED, r2, ALIGNED, ALIGNED, lora2, H, scratch, scratch_bytes, M, N, K, r, None,
+        None)
+
+
 def _awq(M=1, N=64, K=256, g=64, X=ALIGNED):
     return lib.raw_lib().awq_gemv_w4a16(X, ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, M, N, K, g,
                                         None, None)
@@ -124,6 +134,19 @@ def test_qkv_argument_errors():
     assert _qkv(M=0, nq=P(0)) == 0
 
 
+def test_gelu_quant_argument_errors():
+    assert _gq(N=128) == -2 and _gq(N=384) == -2   # whole 256-column tiles only
+    assert _gq(K=200) == -2 and _gq(M=-1) == -2
+    assert _gq(r=8) == -6 and _gq(r2=16) == -6 and _gq(r2=48) == -6
+    assert _gq(inv2=P(0)) == -1 and _gq(scratch=P(0)) == -1 and _gq(lora2=P(0)) == -1
+    assert _gq(scratch_bytes=lib.gelu_quant_scratch_bytes(64, 256, 32) - 1) == -2
+    assert _gq(M=300, N=512, r2=64,
+               scratch_bytes=lib.gelu_quant_scratch_bytes(300, 512, 64) - 16) == -2
+    assert lib.gelu_quant_scratch_bytes(4096, 12288, 32) == (128 + 16) * 256 * 32 * 4
+    assert _gq(inv2=MISALIGNED) == -3 and _gq(H=MISALIGNED) == -3
+    assert _gq(M=0, inv2=P(0), scratch_bytes=0) == 0
+
+
 def test_awq_argument_errors():
     assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(g=128) == -2
     assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
@@ -134,7 +157,8 @@ def test_awq_argument_errors():
 @pytest.mark.skipif(HAS_GPU, reason="valid arguments would launch on a real device")
 def test_device_calls_without_device_report_cuda_error():
     assert _qa() == -5 and _gemm() == -5 and _awq() == -5
-    assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5 and _qkv() == -5
+    assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5 and _qkv() == -5 and _gq() == -5
+    assert _gq(H=ALIGNED) == -5
 
 
 # ------------------------------------------------------------- host packers
