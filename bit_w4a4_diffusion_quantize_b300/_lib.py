@@ -53,6 +53,9 @@ _SIGS = {
     "svdq_gemm_w4a4_gelu_quant": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p,
                                          _c_p, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p,
                                          ctypes.c_size_t, _i32, _i32, _i32, _i32, _c_p, _c_p]),
+    "svdq_gemm_w4a4_gelu_quant_static": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p,
+                                                _c_p, _c_p, _c_p, _i32, _c_p, _c_p, _c_p, _c_p,
+                                                _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "awq_gemv_w4a16": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _i32, _i32,
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
@@ -351,6 +354,51 @@ def svdq_gemm_w4a4_gelu_quant(a_codes, a_scales, w_codes, w_scales, w_tensor_sca
         int(scratch_bytes), int(M), int(N), int(K), int(rank), _dptr(dev_status),
         _stream_ptr(stream))
     _check(st, "svdq_gemm_w4a4_gelu_quant")
+    return a2_codes, a2_scales, lora_act2
+
+
+GELU_QUANT_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def svdq_gemm_w4a4_gelu_quant_static(a_codes, a_scales, w_codes, w_scales,
+                                     w_tensor_scale: float, lora_act, L2s, bias, inv_lambda2,
+                                     L1s2, rank2: int, M: int, N: int, K: int, rank: int,
+                                     a2_codes, a2_scales, lora_act2, H=None, dev_status=None,
+                                     stream=None):
+    """svdq_gemm_w4a4_gelu_quant with the library's static device scratch
+    (include/svdq.h): nothing is allocated, here or in the library, so every
+    output must be passed.  Calls on one device must not overlap in time."""
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2s, "L2s"), (bias, "bias"),
+                 (inv_lambda2, "inv_lambda2"), (L1s2, "L1s2"), (a2_codes, "a2_codes"),
+                 (a2_scales, "a2_scales"), (lora_act2, "lora_act2"), (H, "H"),
+                 (dev_status, "dev_status")):
+        _check_cuda(t, n)
+    if M > 0:
+        for t, n, e, z in ((a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", scale_bytes(M, K), 1),
+                           (w_codes, "w_codes", code_bytes(N, K), 1),
+                           (w_scales, "w_scales", scale_bytes(N, K), 1),
+                           (lora_act, "lora_act", M * rank, 2), (L2s, "L2s", N * rank, 2),
+                           (bias, "bias", N, 2), (inv_lambda2, "inv_lambda2", N, 4),
+                           (L1s2, "L1s2", rank2 * N, 2),
+                           (a2_codes, "a2_codes", code_bytes(M, N), 1),
+                           (a2_scales, "a2_scales", scale_bytes(M, N), 1),
+                           (lora_act2, "lora_act2", M * rank2, 2), (H, "H", M * N, 2),
+                           (dev_status, "dev_status", 1, 4)):
+            if t is None and n not in ("bias", "H", "dev_status"):
+                raise ValueError(f"{n}: required (this call allocates nothing)")
+            _need(t, n, e, z)
+    if gelu_quant_scratch_bytes(M, N, rank2) > GELU_QUANT_STATIC_SCRATCH_BYTES and rank2 in (32, 64):
+        raise SvdqError(-2, f"svdq_gemm_w4a4_gelu_quant_static: M = {M} needs "
+                            f"{gelu_quant_scratch_bytes(M, N, rank2)} bytes of scratch, the "
+                            f"static scratch holds {GELU_QUANT_STATIC_SCRATCH_BYTES}")
+    st = _lib.svdq_gemm_w4a4_gelu_quant_static(
+        _dptr(a_codes), _dptr(a_scales), _dptr(w_codes), _dptr(w_scales), float(w_tensor_scale),
+        _dptr(lora_act), _dptr(L2s), _dptr(bias), _dptr(inv_lambda2), _dptr(L1s2), int(rank2),
+        _dptr(a2_codes), _dptr(a2_scales), _dptr(lora_act2), _dptr(H), int(M), int(N), int(K),
+        int(rank), _dptr(dev_status), _stream_ptr(stream))
+    _check(st, "svdq_gemm_w4a4_gelu_quant_static")
     return a2_codes, a2_scales, lora_act2
 
 

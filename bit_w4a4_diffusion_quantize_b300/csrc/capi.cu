@@ -326,6 +326,69 @@ svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,
 
 }  // extern "C"
 
+namespace {
+
+// Scratch of svdq_gemm_w4a4_gelu_quant_static: one fixed array in device
+// global memory, part of this library's device image (it exists on a device
+// once the library's kernels are loaded there), shared by every call on that
+// device.  Its address is looked up once per device.
+static __device__ __align__(256) float g_gq_static_scratch[SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES /
+                                                           sizeof(float)];
+std::atomic<float*> g_gq_static_ptr[kMaxDevices];
+std::mutex g_gq_static_mu;
+
+float* gq_static_scratch(int dev) {
+  float* p = g_gq_static_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_gq_static_mu);
+  p = g_gq_static_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_gq_static_scratch) != cudaSuccess || !a) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    p = static_cast<float*>(a);
+    g_gq_static_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+}  // namespace
+
+extern "C" svdq_status svdq_gemm_w4a4_gelu_quant_static(
+    const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+    const uint8_t* w_scales, float w_tensor_scale, const uint16_t* lora_act, const uint16_t* L2s,
+    const uint16_t* bias, const float* inv_lambda2, const uint16_t* L1s2, int rank2,
+    uint8_t* a2_codes, uint8_t* a2_scales, uint16_t* lora_act2, uint16_t* H, int M, int N, int K,
+    int rank, int* dev_status, void* stream) {
+  if (M < 0 || N <= 0 || N % 256 != 0) return SVDQ_ERR_SHAPE;
+  if (rank2 != 32 && rank2 != 64) return SVDQ_ERR_RANK;
+  if (SVDQ_GELU_QUANT_SCRATCH_BYTES(M, N, rank2) > SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES)
+    return SVDQ_ERR_SHAPE;  // more rows than the static scratch holds
+  if (M == 0)
+    return svdq_gemm_w4a4_gelu_quant(a_codes, a_scales, w_codes, w_scales, w_tensor_scale,
+                                     lora_act, L2s, bias, inv_lambda2, L1s2, rank2, a2_codes,
+                                     a2_scales, lora_act2, H, nullptr, 0, M, N, K, rank,
+                                     dev_status, stream);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SVDQ_ERR_CUDA;
+  }
+  // (the architecture check first: the device image holding the array loads
+  // only on a supported device)
+  svdq_status st = current_device(nullptr, nullptr);
+  if (st != SVDQ_OK) return st;
+  float* scratch = gq_static_scratch(dev);
+  if (!scratch) return SVDQ_ERR_CUDA;
+  return svdq_gemm_w4a4_gelu_quant(a_codes, a_scales, w_codes, w_scales, w_tensor_scale,
+                                   lora_act, L2s, bias, inv_lambda2, L1s2, rank2, a2_codes,
+                                   a2_scales, lora_act2, H, scratch,
+                                   SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES, M, N, K, rank,
+                                   dev_status, stream);
+}
+
 extern "C" svdq_status svdq_test_set_hooks(int fake_compute_capability, int gemm_stall) {
   if (fake_compute_capability < 0 || (gemm_stall != 0 && gemm_stall != 1)) return SVDQ_ERR_VALUE;
   g_fake_cc.store(fake_compute_capability, std::memory_order_relaxed);

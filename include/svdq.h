@@ -275,6 +275,40 @@ svdq_status svdq_gemm_w4a4_gelu_quant(const uint8_t* a_codes, const uint8_t* a_s
                                       size_t scratch_bytes, int M, int N, int K, int rank,
                                       int* dev_status, void* stream);
 
+/* svdq_gemm_w4a4_gelu_quant without caller scratch: the scratch is a fixed
+ * array of SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES in device global memory that
+ * belongs to this library (loaded with its kernels, one per device, never
+ * allocated or freed by the call).  This call has no counterpart in the
+ * method's description; it exists for callers that cannot allocate device
+ * memory at the point of the call: a runtime with a fixed device-memory
+ * budget that hands out no scratch, or a loop that must never block on or
+ * fail in an allocator.
+ * Limits and rules:
+ *   - SVDQ_GELU_QUANT_SCRATCH_BYTES(M, N, rank2) must not exceed
+ *     SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES: rank2 32 allows M <= 98304,
+ *     rank2 64 allows M <= 32768 (SVDQ_ERR_SHAPE beyond).
+ *   - The first call on a device (that device current) looks up the array's
+ *     address (cudaGetSymbolAddress, which may load the library's device
+ *     code): make one call on each device before any stream capture.
+ *     SVDQ_ERR_CUDA if the lookup fails.
+ *   - Nothing in the array needs to start at zero: a call writes every part
+ *     it later reads.
+ *   - Every call on a device uses the same array: two calls whose work
+ *     overlaps in time (different streams, or different host threads on
+ *     unsynchronised streams) race on it and give wrong results.  Order the
+ *     calls on one stream, or use svdq_gemm_w4a4_gelu_quant with separate
+ *     scratch buffers.
+ * Everything else (arguments, outputs, sizes, errors) is that of
+ * svdq_gemm_w4a4_gelu_quant. */
+#define SVDQ_GELU_QUANT_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+svdq_status svdq_gemm_w4a4_gelu_quant_static(
+    const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* w_codes,
+    const uint8_t* w_scales, float w_tensor_scale, const uint16_t* lora_act,
+    const uint16_t* L2s, const uint16_t* bias, const float* inv_lambda2,
+    const uint16_t* L1s2, int rank2, uint8_t* a2_codes, uint8_t* a2_scales,
+    uint16_t* lora_act2, uint16_t* H, int M, int N, int K, int rank, int* dev_status,
+    void* stream);
+
 /* svdq_gemm_w4a4 for a fused Q|K|V projection, with the normalization of Q and
  * K and the rotary embedding in its epilogue (dothoosh.com, "How Nunchaku Lite
  * halves the VRAM of diffusion models", paragraphs on structural rewrites:

@@ -147,6 +147,20 @@ def test_gelu_quant_argument_errors():
     assert _gq(M=0, inv2=P(0), scratch_bytes=0) == 0
 
 
+def test_gelu_quant_static_argument_errors():
+    raw = lib.raw_lib()
+
+    def call(M=64, N=256, r2=32):
+        return raw.svdq_gemm_w4a4_gelu_quant_static(
+            ALIGNED, ALIGNED, ALIGNED, ALIGNED, ctypes.c_float(2.0 ** -10), ALIGNED, ALIGNED,
+            None, ALIGNED, ALIGNED, r2, ALIGNED, ALIGNED, ALIGNED, None, M, N, 256, 32, None,
+            None)
+    assert call(N=384) == -2 and call(M=-1) == -2 and call(r2=16) == -6
+    assert call(M=98304) != -2 and call(M=98305) == -2            # rank2 32: row limit
+    assert call(M=32768, r2=64) != -2 and call(M=32769, r2=64) == -2
+    assert call(M=0) == 0
+
+
 def test_awq_argument_errors():
     assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(g=128) == -2
     assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
