@@ -760,6 +760,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = mbar_wait(&full[s], (uint32_t)(it / STAGES) & 1u, dev_status, wait_ns) &&
              !*abort_flag;
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        if (warp == SF_WARP0 && lane == 0) SVDQ_TR(960, 64, it);
         const int nkb = min(KB_PER_TILE, kb_total - kt * KB_PER_TILE);
         const uint8_t* sfa = smem + C::OFF_SFA + s * C::SFA_BYTES + lane * 16;
         const uint8_t* sfb = smem + C::OFF_SFB + s * C::SFB_BYTES + lane * 16;
