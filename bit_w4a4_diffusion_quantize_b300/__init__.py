@@ -17,7 +17,7 @@ _LIB_NAMES = {
     "svdq_gemm_w4a4_gelu_quant_static", "GELU_QUANT_STATIC_SCRATCH_BYTES",
     "svdq_quantize_act", "test_set_hooks",
 }
-_LAYER_NAMES = {"SVDQLinear", "AWQLinear"}
+_LAYER_NAMES = {"SVDQLinear", "SVDQMLP", "AWQLinear"}
 
 __all__ = sorted(_LIB_NAMES | _LAYER_NAMES)
 

@@ -56,6 +56,48 @@ class SVDQLinear:
     __call__ = forward
 
 
+class SVDQMLP:
+    """Y2 = fc2(gelu_tanh(fc1(X))) for two SVDQ linears, fc1.N == fc2.K.  The
+    fused path is three library calls: svdq_quantize_act (fc1's activation
+    side), svdq_gemm_w4a4_gelu_quant (fc1 with GELU and fc2's activation side
+    in its epilogue: H is never written) and svdq_gemm_w4a4 (fc2).
+    fused=False runs fc1 with the GELU epilogue, writes H, and runs fc2 on it
+    (the four-call path), for comparison."""
+
+    def __init__(self, fc1: SVDQLinear, fc2: SVDQLinear):
+        if fc1.N != fc2.K:
+            raise ValueError(f"fc1.N = {fc1.N} must equal fc2.K = {fc2.K}")
+        self.fc1, self.fc2 = fc1, fc2
+        self._scratch = None
+
+    def _scratch_for(self, M, device):
+        import torch
+
+        need = _lib.gelu_quant_scratch_bytes(M, self.fc1.N, self.fc2.rank)
+        if self._scratch is None or self._scratch.numel() < need or \
+                self._scratch.device != device:
+            self._scratch = torch.empty(need, dtype=torch.uint8, device=device)
+        return self._scratch
+
+    def forward(self, X, out=None, fused=True, dev_status=None, stream=None):
+        fc1, fc2 = self.fc1, self.fc2
+        M = X.shape[0]
+        if not fused:
+            H = fc1(X, gelu=True, dev_status=dev_status, stream=stream)
+            return fc2(H, out=out, dev_status=dev_status, stream=stream)
+        a_codes, a_scales, lora = _lib.svdq_quantize_act(
+            X, fc1.inv_lambda, fc1.L1s, fc1.rank, dev_status=dev_status, stream=stream)
+        a2_codes, a2_scales, lora2 = _lib.svdq_gemm_w4a4_gelu_quant(
+            a_codes, a_scales, fc1.w_codes, fc1.w_scales, fc1.w_tensor_scale, lora, fc1.L2s,
+            fc1.bias, fc2.inv_lambda, fc2.L1s, fc2.rank, M, fc1.N, fc1.K, fc1.rank,
+            scratch=self._scratch_for(M, X.device), dev_status=dev_status, stream=stream)
+        return _lib.svdq_gemm_w4a4(a2_codes, a2_scales, fc2.w_codes, fc2.w_scales,
+                                   fc2.w_tensor_scale, lora2, fc2.L2s, fc2.bias, M, fc2.N,
+                                   fc2.K, fc2.rank, out, dev_status=dev_status, stream=stream)
+
+    __call__ = forward
+
+
 class AWQLinear:
     """Y = awq_gemv_w4a16(X) for a weight packed by awq_pack_weights."""
 

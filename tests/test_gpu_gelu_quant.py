@@ -183,3 +183,33 @@ def test_gelu_quant_mlp_full_size():
     rows = np.sort(np.random.default_rng(61).choice(M, 256, replace=False))
     _check_quant(a2c, a2s, h, p2["inv_lambda"], rows)
     _check_lora2(host_bf16(l2)[rows], h[rows], p2["L1s"])
+
+
+def test_mlp_layer_fused_against_oracle_and_unfused():
+    """SVDQMLP (the user-level path: K1, the fused GELU + quantization GEMM,
+    fc2's GEMM) on weights packed by svdq_pack_weights, fc2 calibrated on H:
+    the fused and the unfused (H written, then fc2's own K1) outputs each
+    against the oracle's fc2 forward of the device's H on those packed
+    weights."""
+    from test_gpu_linear import _oracle_view_of_product_packing
+    from gpu_util import assert_y_close, lora_rounding_slack
+
+    M, K, N1, N2, r = 300, 256, 512, 256, 32
+    c1 = workloads.custom_case(M, K, N1, r, seed=41)
+    X = workloads.make_activations(c1)
+    W1, b1 = workloads.make_weights(c1)
+    W2, b2 = workloads.make_weights(workloads.custom_case(M, N1, N2, r, seed=42))
+    fc1 = lib.SVDQLinear.from_float(W1, lib.svdq_calib_absmax(workloads.bf16_bits_of(X)), r,
+                                    bias_bf16_bits=workloads.bf16_bits_of(b1))
+    Xd = dev_bf16(X)
+    h = host_bf16(fc1(Xd, gelu=True))
+    p2 = lib.svdq_pack_weights(W2, lib.svdq_calib_absmax(workloads.bf16_bits_of(h)), r)
+    fc2 = lib.SVDQLinear(p2, workloads.bf16_bits_of(b2))
+    mlp = lib.SVDQMLP(fc1, fc2)
+    y_fused = host_bf16(mlp(Xd))
+    y_unfused = host_bf16(mlp(Xd, fused=False))
+    view = _oracle_view_of_product_packing(p2)
+    ref = svdq.linear_forward(h, view, b2)["Y"]
+    slack = lora_rounding_slack(h, view["L1s"], view["L2"])
+    assert_y_close(y_fused, ref, "MLP fused (fc2 Y)", slack)
+    assert_y_close(y_unfused, ref, "MLP unfused (fc2 Y)", slack)
