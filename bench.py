@@ -376,6 +376,12 @@ def run_gpu(args, world, rank, local):
     e2e = {"value": world * args.steps * flop / t_e2e / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
            "ms_per_step": t_e2e / args.steps * 1e3}
+    # the host link on its own: the step's two copies timed alone (pinned
+    # memory, this stream), and the share of a step they account for
+    link = host_link(Xh, Xd, Yd, Yh, stream, reps=max(3, min(args.steps, 20)))
+    e2e["host_link"] = link
+    e2e["copies_share_of_step"] = round(
+        (link["h2d_ms"] + link["d2h_ms"]) / e2e["ms_per_step"], 3)
     try:
         e2e_pipe = e2e_pipelined(args, layer, Xbits, M, K, N, dev, stream, bufs, world, flop)
     except Exception as exc:  # reported in the line; the serial e2e above stands alone
@@ -384,6 +390,9 @@ def run_gpu(args, world, rank, local):
         except Exception:
             pass
         e2e_pipe = {"error": f"{type(exc).__name__}: {exc}"}
+    if "error" not in e2e_pipe:
+        # with the two directions on their own streams, the longer copy bounds a step
+        e2e_pipe["copies_bound_ms_per_step"] = max(link["h2d_ms"], link["d2h_ms"])
 
     # ---- AWQ W4A16: the stacked modulation GEMVs
     awq = None
@@ -664,6 +673,29 @@ def run_mlp_gelu(args, lib, dev, stream, world):
     res["gelu_quant_saving"] = round(1.0 - res["us_gelu_quant"] /
                                      res["us_gelu_then_quantize_act"], 4)
     return res
+
+
+def host_link(Xh, Xd, Yd, Yh, stream, reps):
+    """GB/s of the host-to-device copy of X and the device-to-host copy of Y
+    (pinned host buffers), each timed alone with CUDA events on `stream`."""
+    import torch
+    out = {}
+    for name, dst, src in (("h2d", Xd, Xh), ("d2h", Yh, Yd)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = src.numel() * src.element_size()
+        out[f"{name}_ms"] = round(ms, 4)
+        out[f"{name}_gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return out
 
 
 def e2e_pipelined(args, layer, Xbits, M, K, N, dev, stream, bufs, world, flop):
