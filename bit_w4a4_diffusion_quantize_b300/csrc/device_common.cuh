@@ -213,6 +213,12 @@ SVDQ_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, in
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// hint: bring a 2-D box of a tensor map into L2 (no data comes back)
+SVDQ_DEVINL void tma_prefetch_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
+               "r"(x), "r"(y)
+               : "memory");
+}
 // 3-D tiled bulk tensor load global -> shared, completion on an mbarrier.
 SVDQ_DEVINL void tma_load_3d(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y,
                              int z) {

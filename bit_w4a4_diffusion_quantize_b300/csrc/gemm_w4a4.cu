@@ -461,6 +461,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   grid_dep_launch();
+  // The weight side is no output of the previous kernel: ask L2 for this
+  // CTA's half of the first tile's W rows and their scales now (hints only),
+  // while that kernel may still run.
+  if (warp == 0 && lane == 0 && my_tiles > 0) {
+    int m_tile, n_tile;
+    tile_mn(0, m_tile, n_tile);
+    const int n0 = n_tile * BN, nh = n0 + (int)crank * C::BH;
+    const int kp = min(k_tiles, 2 * STAGES);
+    for (int kt = 0; kt < kp; ++kt) tma_prefetch_2d(&tm_b, kt * BK_BYTES, nh);
+    for (int h = 0; h < BN / 128; ++h)
+      bulk_prefetch_l2(w_scales + (size_t)(n0 / 128 + h) * kb_total * 512,
+                       (uint32_t)(min(kb_total, kp * KB_PER_TILE) * 512));
+  }
   grid_dep_wait();  // the previous kernel's outputs (our inputs) are complete
 
   int issued = 0;  // producer lane only: ring slots filled
