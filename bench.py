@@ -51,19 +51,21 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio of the tensor cores
 # sources hash to what was captured (the summaries are under profiles/).
 MEASURED_TRAFFIC = {
     "svdq_gemm_w4a4": {
-        "bytes": 12889600 + 3840,
-        "sources": {"gemm_w4a4.cu": "d7ad3de4a2d5ad21afa9c7fa13715414b78b00ae06f82425dbee6f2e00f65dc7",
-                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
+        "bytes": 12891392 + 0,
+        "sources": {"gemm_w4a4.cu": "ac19a0cc97be41595b5d2022d45f0c360f4186ac3c64f98633625d3addd596dd",
+                    "act_quant.cuh": "bea739112402fcfe84521d48b6e661028f64613e645ba281febb8147d55b1520",
+                    "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
     "svdq_quantize_act": {
-        "bytes": 25391616 + 0,
-        "sources": {"quantize_act.cu": "1ac727eb664eed2921ff4941ba6decbc109f896b8bda3fa0f110429d2869aac9",
-                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
+        "bytes": 25392640 + 0,
+        "sources": {"quantize_act.cu": "5ee00dc9b9856827a5d5a78b1a154ed8a6e2a67db920f8bf4f7d729272846aff",
+                    "act_quant.cuh": "bea739112402fcfe84521d48b6e661028f64613e645ba281febb8147d55b1520",
+                    "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
-        "bytes": 31935488 + 0,
+        "bytes": 31937280 + 0,
         "sources": {"awq_gemv.cu": "59c214c33078bf99e64d0086c8b1bb568d561ed08180de56c4fe71080abba856",
-                    "device_common.cuh": "92fdfafe5e74dcf624a4babca80c30dfd83c2d614e887d1aeef52157401dc14a"},
+                    "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/awq_gemv_w4a16_modulation_ncu.md"},
 }
 
