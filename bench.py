@@ -63,8 +63,8 @@ MEASURED_TRAFFIC = {
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
-        "bytes": 31937280 + 0,
-        "sources": {"awq_gemv.cu": "59c214c33078bf99e64d0086c8b1bb568d561ed08180de56c4fe71080abba856",
+        "bytes": 31934464 + 0,
+        "sources": {"awq_gemv.cu": "cc0f366eeff3794b51fa8afa39adfe5516d626fb278178ce229587cf12f163d8",
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/awq_gemv_w4a16_modulation_ncu.md"},
 }

@@ -122,13 +122,15 @@ __global__ void __launch_bounds__(32 * (CW + 1), 1)
     abort_flag = 0;
     fence_mbar_init();
   }
-  // The weights of this CTA's tiles are read-only operands: ask L2 for all of
+  // The weights of this CTA's first tiles are read-only operands: ask L2 for
   // them now (hints only, no data comes back), before the wait for the
   // previous kernel, so that the stream from HBM starts with the launch and
-  // the loads below find L2 lines.
+  // the first loads find L2 lines.  (Asking for all of the CTA's tiles at
+  // once measured slower: 14.4 against 13.8 us per 57-block launch.)
+  constexpr int kPrefetchTiles = 2;
   if (threadIdx.x == 32 * CW) {
     const size_t row_bytes = (size_t)K / 2;
-    for (int j = 0; j < my_tiles; ++j) {
+    for (int j = 0; j < my_tiles && j < kPrefetchTiles; ++j) {
       const int n0 = (blockIdx.x + j * gridDim.x) * 16;
       const int rows = min(16, N - n0);
       bulk_prefetch_l2(qw + (size_t)n0 * row_bytes, (uint32_t)(rows * row_bytes));
