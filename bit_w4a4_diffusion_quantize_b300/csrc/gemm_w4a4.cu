@@ -16,6 +16,14 @@
 //      and turned pair by pair by the tokens' rotary angles, V as Y (same
 //      article, structural rewrites: one fused operator for the QKV
 //      projection, the Q/K normalization and the rotary embeddings)
+//   or the GELU + quantization variant: H as the GELU variant, quantized as
+//      the next linear's input (its e2m1 codes and e4m3 scales, with its
+//      inv_lambda) and multiplied by the next linear's L1s on the tensor
+//      cores (its low-rank down projection, summed per CTA pair over the
+//      pair's run of tiles of one 256-row block; a second kernel adds the
+//      runs), H written only on request (same article, the full engine's
+//      GELU/MLP kernels; the fused-kernel paragraph: down projection with
+//      the quantization)
 //
 // Persistent kernel in clusters of two CTAs (one CTA per SM) that compute
 // together with the tensor cores' CTA-pair MMAs (tcgen05 cta_group::2).  A
@@ -28,7 +36,8 @@
 // 16 KB, block scales 6 KB) for the same 16.8 MFLOP that a lone 128 x 256
 // tile would need 54 KB for.
 //
-// Each CTA's ring (5 slots of 38 KB at BN = 256) carries, per output tile,
+// Each CTA's ring (4 slots of 38 KB at BN = 256; 5 for the QKV variant, whose
+// epilogue needs no staging area) carries, per output tile,
 // its k tiles -- A code tile and its scale chunk, the CTA's half of the W code
 // rows, and the scale chunks of all BN W rows (both halves: the MMA of each
 // SM needs every column's scales in its own TMEM); 128-byte rows, 128B
