@@ -15,7 +15,7 @@ _LIB_NAMES = {
     "svdq_calib_absmax", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu", "svdq_gemm_w4a4_qkv",
     "svdq_gemm_w4a4_gelu_quant", "gelu_quant_scratch_bytes", "svdq_pack_weights",
     "svdq_gemm_w4a4_gelu_quant_static", "GELU_QUANT_STATIC_SCRATCH_BYTES",
-    "svdq_quantize_act", "test_set_hooks",
+    "svdq_quantize_act", "test_set_hooks", "test_quant_sweep",
 }
 _LAYER_NAMES = {"SVDQLinear", "SVDQMLP", "AWQLinear"}
 

@@ -60,6 +60,7 @@ _SIGS = {
                               _c_p, _c_p]),
     "svdq_bench_mma_rate": (_i32, [_i32, _i32, _i32, _i32, _c_p, _c_p]),
     "svdq_test_set_hooks": (_i32, [_i32, _i32]),
+    "svdq_test_quant_sweep": (_i32, [_i32, _c_p, _c_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -438,3 +439,16 @@ def test_set_hooks(fake_compute_capability: int = 0, gemm_stall: int = 0):
     loader that issues nothing (1), so that its bounded waits run out."""
     _check(_lib.svdq_test_set_hooks(int(fake_compute_capability), int(gemm_stall)),
            "svdq_test_set_hooks")
+
+
+def test_quant_sweep(which: int, stream=None):
+    """Run the exhaustive rounding check (include/svdq_test.h); returns
+    (mismatching blocks, smallest mismatching fp32 bit pattern or None,
+    blocks checked)."""
+    torch = _torch()
+    out = torch.tensor([0, -1, 0, 0], dtype=torch.int64, device="cuda")
+    _check(_lib.svdq_test_quant_sweep(int(which), _dptr(out), _stream_ptr(stream)),
+           "svdq_test_quant_sweep")
+    torch.cuda.synchronize()
+    count, first, checked, _ = (int(v) for v in out.cpu().tolist())
+    return count, (None if count == 0 else first & 0xFFFFFFFF), checked

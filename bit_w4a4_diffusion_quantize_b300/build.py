@@ -17,7 +17,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsvdq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu", "microbench.cu"]
+CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu", "microbench.cu",
+                "selftest.cu"]
 HOST_SOURCES = ["pack.cpp"]
 HEADERS = ["device_common.cuh", "act_quant.cuh", "launch.h"]
 

@@ -145,3 +145,15 @@ def test_quantize_act_repeatable():
     # padding rows of the scale tiles are never written: compare the real rows
     assert np.array_equal(scales_from_device(a[1], 200, 512), scales_from_device(b[1], 200, 512))
     assert np.array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("which", [0, 1], ids=["scales_all_fp32", "codes_every_scale"])
+def test_exact_quotient_rounding_exhaustive(which):
+    """The library's division-free rounding (shared by svdq_quantize_act and
+    the fused GELU + quantization epilogue) against IEEE division followed by
+    the same RNE conversion -- the exact rounding of the quotient -- over every
+    finite fp32 amax (scale bytes), and over every e4m3 scale with every fp32
+    value in the top 8 binades below its block amax, both signs (codes)."""
+    count, first, checked = lib.test_quant_sweep(which)
+    assert checked == (0x7F800000 if which == 0 else 126 * -(-(1 << 26) // 7)), checked
+    assert count == 0, f"{count} blocks differ; smallest fp32 pattern {first:#010x}"

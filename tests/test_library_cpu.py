@@ -44,6 +44,13 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(raw, n), n
 
 
+def test_quant_sweep_argument_errors():
+    raw = lib.raw_lib()
+    assert raw.svdq_test_quant_sweep(2, ALIGNED, None) == -7
+    assert raw.svdq_test_quant_sweep(0, None, None) == -1
+    assert raw.svdq_test_quant_sweep(0, MISALIGNED, None) == -3
+
+
 def test_test_hooks_refuse_bad_values_and_reset():
     raw = lib.raw_lib()
     assert raw.svdq_test_set_hooks(-1, 0) == -7
