@@ -1067,7 +1067,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 __device__ __forceinline__ int gq_owner(int t, int num_ptiles, int n_pairs) {
   return (int)(((unsigned)(t + 1) * (unsigned)n_pairs - 1u) / (unsigned)num_ptiles);
 }
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(128, 4)
     k_lora_reduce(const float* __restrict__ partial, int M, int rank2, int num_ptiles,
                   int n_pairs, int n_tiles, uint16_t* __restrict__ lora2) {
   grid_dep_launch();
@@ -1155,9 +1155,12 @@ cudaError_t launch_t(const GemmMaps& maps, const uint8_t* a_scales, const uint8_
   if (EPI == kEpiGeluQuant) {
     cudaLaunchConfig_t rc = {};
     const size_t total = (size_t)M * (gq.rank2 / 4);
-    const size_t blocks = (total + 255) / 256;
+    // small blocks: one fits on an SM beside a GEMM CTA (registers), so the
+    // reduction's blocks wait resident during the GEMM, and the next kernel's
+    // GEMM CTAs can start beside them
+    const size_t blocks = (total + 127) / 128;
     rc.gridDim = dim3((unsigned)(blocks < 4096 ? blocks : 4096), 1, 1);
-    rc.blockDim = dim3(256, 1, 1);
+    rc.blockDim = dim3(128, 1, 1);
     rc.stream = stream;
     rc.attrs = &attr[1];  // programmatic dependent launch
     rc.numAttrs = 1;
