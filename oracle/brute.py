@@ -125,3 +125,91 @@ def gemm_exact(a_codes, a_scales, w_codes, w_scales, s_T, lora_act, L2, bias):
             row.append(y)
         Y.append(row)
     return Y
+
+
+# ---------------------------------------------------------------- INT4 variant
+def round_binary(value: Fraction, mant_bits: int, emin: int = -126) -> Fraction:
+    """Nearest number with ``mant_bits`` significant bits, exponent >= emin
+    (below it: the fixed subnormal spacing 2^(emin - mant_bits + 1)), ties to
+    an even last digit.  binary32: (24, -126); bfloat16: (8, -126).  No
+    overflow (the callers' values stay far below the largest finite one)."""
+    if value == 0:
+        return Fraction(0)
+    a = abs(value)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, emin) - (mant_bits - 1))
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * quantum
+    return -r if value < 0 else r
+
+
+def round_half_even_int(value: Fraction) -> int:
+    fl = value.numerator // value.denominator
+    rem = value - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+def int4_codes(values, s: Fraction):
+    """Symmetric 4-bit integer codes of exact values under scale s (0 -> 0)."""
+    if s == 0:
+        return [0] * len(values)
+    return [max(-8, min(7, round_half_even_int(v / s))) for v in values]
+
+
+def int4_act_row(x_row, inv_lambda):
+    """One activation row (floats exactly bf16) -> (codes, scales as
+    Fractions): x_hat = fl32(x inv), s = bf16(fl32(amax / 7)) per 64 k."""
+    xhat = [Fraction(f32(float(x) * float(il))) for x, il in zip(x_row, inv_lambda)]
+    codes, scales = [], []
+    for g in range(0, len(xhat), 64):
+        blk = xhat[g:g + 64]
+        amax = max(abs(v) for v in blk)
+        s = round_binary(round_binary(amax / 7, 24), 8)
+        scales.append(s)
+        codes += int4_codes(blk, s)
+    return codes, scales
+
+
+def int4_weight_col(r_col):
+    """One output channel of the float64 residual -> (codes, scales):
+    s = bf16(amax / 7) of the exact quotient per 64 k."""
+    vals = [Fraction(v) for v in r_col]
+    codes, scales = [], []
+    for g in range(0, len(vals), 64):
+        blk = vals[g:g + 64]
+        s = round_binary(max(abs(v) for v in blk) / 7, 8)
+        scales.append(s)
+        codes += int4_codes(blk, s)
+    return codes, scales
+
+
+def int4_gemm_exact(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias):
+    """Exact Y of the INT4 layer from codes and group scales (Fractions or
+    floats); L2 is [r][N]."""
+    M, N = len(a_codes), len(w_codes)
+    K = len(a_codes[0]) if M else 0
+    Y = []
+    for m in range(M):
+        row = []
+        for n in range(N):
+            y = Fraction(0)
+            for g in range(K // 64):
+                isum = sum(int(a_codes[m][k]) * int(w_codes[n][k]) for k in range(64 * g, 64 * g + 64))
+                y += Fraction(a_scales[m][g]) * Fraction(w_scales[n][g]) * isum
+            for i in range(len(L2)):
+                y += Fraction(lora_act[m][i]) * Fraction(L2[i][n])
+            if bias is not None:
+                y += Fraction(bias[n])
+            row.append(y)
+        Y.append(row)
+    return Y
