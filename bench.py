@@ -57,11 +57,24 @@ MEASURED_TRAFFIC = {
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_gemm_w4a4_attn_out_ncu.md"},
     "svdq_quantize_act": {
-        "bytes": 25392640 + 0,
-        "sources": {"quantize_act.cu": "5ee00dc9b9856827a5d5a78b1a154ed8a6e2a67db920f8bf4f7d729272846aff",
+        "bytes": 25392128 + 0,
+        "sources": {"quantize_act.cu": "d0998b9fff12f198db08792f7ce47d2c9cf9e804fa3f37fad0e7afd06ea2da2e",
                     "act_quant.cuh": "bea739112402fcfe84521d48b6e661028f64613e645ba281febb8147d55b1520",
+                    "int4_quant.cuh": "a4a9954f799df30b652ac915d56273d1f9ef5b94d2ec3dbc03eaafcd92a4dc09",
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_quantize_act_attn_out_ncu.md"},
+    "svdq_quantize_act_int4": {
+        "bytes": 25395328 + 0,
+        "sources": {"quantize_act.cu": "d0998b9fff12f198db08792f7ce47d2c9cf9e804fa3f37fad0e7afd06ea2da2e",
+                    "act_quant.cuh": "bea739112402fcfe84521d48b6e661028f64613e645ba281febb8147d55b1520",
+                    "int4_quant.cuh": "a4a9954f799df30b652ac915d56273d1f9ef5b94d2ec3dbc03eaafcd92a4dc09",
+                    "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
+        "profile": "profiles/svdq_gemm_w4a4_int4_attn_out_ncu.md"},
+    "svdq_gemm_w4a4_int4": {
+        "bytes": 12192256 + 6656,
+        "sources": {"gemm_int4.cu": "1283e16e5c3491e374159d469c4a1f22ec662c02f2db7e3fd7a46b9669f75bcc",
+                    "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
+        "profile": "profiles/svdq_gemm_w4a4_int4_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
         "bytes": 31934464 + 0,
         "sources": {"awq_gemv.cu": "cc0f366eeff3794b51fa8afa39adfe5516d626fb278178ce229587cf12f163d8",
@@ -491,6 +504,10 @@ def run_gpu(args, world, rank, local):
         qk = run_qkv_epilogue(args, lib, dev, stream, world)
         line["qkv_norm_rope"] = qk
         line["gpu_launches"] += qk["launches"]
+    if not args.no_int4:
+        i4 = run_int4(args, lib, dev, stream, world)
+        line["int4"] = i4
+        line["gpu_launches"] += i4["launches"]
     return line
 
 
@@ -583,6 +600,91 @@ def run_qkv_epilogue(args, lib, dev, stream, world):
     res["epilogue_cost"] = round(res["us_fused"] / res["us_plain"] - 1.0, 4)
     res["separate_pass_bytes_avoided"] = 2 * 2 * M * (2 * N // 3) * 2
     return res
+
+
+def run_int4(args, lib, dev, stream, world):
+    """The INT4 variant at the attention out-projection shape (M = 4096,
+    K = N = 3072, rank 32): svdq_quantize_act_int4 and svdq_gemm_w4a4_int4,
+    each alone and as the layer's step, weights from svdq_pack_weights_int4
+    (three input, weight and output sets rotated, > L2 in all).  The GEMM's
+    denominator is the rate of the warp-level e4m3 MMA it runs on, measured
+    here (svdq_bench_mma_rate mode 7); the quantizer's is the HBM copy rate."""
+    import torch
+    case = workloads.CASES["attn_out"]
+    M, K, N, r = case.M, case.K, case.N, case.rank
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    Xbits = workloads.bf16_bits_of(X)
+    t0 = time.perf_counter()
+    packed = lib.svdq_pack_weights_int4(W, lib.svdq_calib_absmax(Xbits), r)
+    pack_s = time.perf_counter() - t0
+
+    def dbits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    inv = torch.from_numpy(packed["inv_lambda"]).to(dev)
+    L1s = dbits(packed["L1s"])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sets = []
+    for _ in range(3):
+        sets.append({
+            "X": dbits(Xbits).view(M, K), "wc": torch.from_numpy(packed["w_codes"]).to(dev),
+            "ws": dbits(packed["w_scales"]), "L2": dbits(packed["L2"]),
+            "bias": dbits(workloads.bf16_bits_of(b)),
+            "ac": torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+            "as": torch.empty((M, K // 64), dtype=torch.bfloat16, device=dev),
+            "lora": torch.empty((M, r), dtype=torch.bfloat16, device=dev),
+            "Y": torch.empty((M, N), dtype=torch.bfloat16, device=dev)})
+
+    def quant(s, st):
+        lib.svdq_quantize_act_int4(s["X"], inv, L1s, r, s["ac"], s["as"], s["lora"],
+                                   dev_status=status, stream=st)
+
+    def gemm(s, st):
+        lib.svdq_gemm_w4a4_int4(s["ac"], s["as"], s["wc"], s["ws"], s["lora"], s["L2"],
+                                s["bias"], M, N, K, r, s["Y"], stream=st)
+
+    def step(s, st):
+        quant(s, st)
+        gemm(s, st)
+
+    def launch(fn, i, st):
+        fn(sets[i % len(sets)], st)
+
+    t_step = _time_graph(args, launch, step, stream, dev, world)
+    t_q = _time_graph(args, launch, quant, stream, dev, world)
+    t_g = _time_graph(args, launch, gemm, stream, dev, world)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the INT4 phase")
+    # the e4m3 warp-MMA rate: 128 m16n8k32 MMAs per CTA and iteration, 8 warps
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    iters = 4096
+    for _ in range(2):
+        lib.bench_mma_rate(7, 128, iters, sms, dev_status=status, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    lib.bench_mma_rate(7, 128, iters, sms, dev_status=status, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warp_mma_tflops = 2.0 * 128 * 128 * 32 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    flop = 2.0 * M * N * K
+    q_bytes = M * K * 2 + M * K // 2 + M * (K // 64) * 2 + M * r * 2
+    gemm_tflops = world * flop / t_g / 1e12
+    hbm = peaks()["hbm_gbs"]
+    return {
+        "workload": f"attn_out, INT4 variant: M={M} K={K} N={N} rank={r}, group 64, bf16 "
+                    f"scales", "launches": 4 * args.steps,
+        "pack_seconds": round(pack_s, 2),
+        "us_step": round(t_step * 1e6, 2), "tflops_step": round(world * flop / t_step / 1e12, 1),
+        "us_quantize_act_int4": round(t_q * 1e6, 2),
+        "quantize_act_int4_gbs": round(q_bytes / t_q / 1e9, 1),
+        "quantize_act_int4_frac_hbm": round(q_bytes / t_q / 1e9 / hbm, 4),
+        "quantize_act_int4_traffic": measured_traffic("svdq_quantize_act_int4"),
+        "us_gemm_int4": round(t_g * 1e6, 2), "tflops_gemm_int4": round(gemm_tflops, 1),
+        "gemm_int4_traffic": measured_traffic("svdq_gemm_w4a4_int4"),
+        "measured_warp_e4m3_mma_tflops": round(warp_mma_tflops, 1),
+        "gemm_int4_frac_of_warp_mma": round(gemm_tflops / warp_mma_tflops, 4),
+    }
 
 
 def run_mlp_gelu(args, lib, dev, stream, world):
@@ -841,6 +943,7 @@ def main(argv=None):
                     help="skip the fc1 + fused GELU phase")
     ap.add_argument("--no-qkv-epilogue", action="store_true",
                     help="skip the QKV + normalization + rotary phase")
+    ap.add_argument("--no-int4", action="store_true", help="skip the INT4 variant's phase")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of repeated steps (untimed) over which clocks are sampled")
     args = ap.parse_args(argv)

@@ -1,4 +1,5 @@
-"""SVDQuant W4A4 (NVFP4) linear layer and AWQ W4A16 GEMV for NVIDIA B300.
+"""SVDQuant W4A4 linear layer (NVFP4, and the INT4 variant) and AWQ W4A16 GEMV
+for NVIDIA B300.
 
 The compute lives in ``libsvdq.so`` (C ABI, ``include/svdq.h``): hand-written
 sm_103a kernels for the per-forward path and C++ host packers for the
@@ -16,8 +17,10 @@ _LIB_NAMES = {
     "svdq_gemm_w4a4_gelu_quant", "gelu_quant_scratch_bytes", "svdq_pack_weights",
     "svdq_gemm_w4a4_gelu_quant_static", "GELU_QUANT_STATIC_SCRATCH_BYTES",
     "svdq_quantize_act", "test_set_hooks", "test_quant_sweep",
+    "svdq_pack_weights_int4", "svdq_quantize_act_int4", "svdq_gemm_w4a4_int4",
+    "int4_scale_bytes",
 }
-_LAYER_NAMES = {"SVDQLinear", "SVDQMLP", "AWQLinear"}
+_LAYER_NAMES = {"SVDQLinear", "SVDQLinearInt4", "SVDQMLP", "AWQLinear"}
 
 __all__ = sorted(_LIB_NAMES | _LAYER_NAMES)
 

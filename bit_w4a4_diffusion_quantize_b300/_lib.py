@@ -42,6 +42,12 @@ _SIGS = {
     "svdq_pack_weights": (_i32, [_c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p,
                                  _c_p]),
     "awq_pack_weights": (_i32, [_c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p]),
+    "svdq_pack_weights_int4": (_i32, [_c_p, _i32, _i32, _c_p, _i32, _c_p, _c_p, _c_p, _c_p,
+                                      _c_p]),
+    "svdq_quantize_act_int4": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p,
+                                      _c_p, _c_p]),
+    "svdq_gemm_w4a4_int4": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32,
+                                   _i32, _i32, _c_p]),
     "svdq_quantize_act": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p,
                                  _c_p]),
     "svdq_gemm_w4a4": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _i32,
@@ -98,6 +104,11 @@ def scale_bytes(rows: int, K: int) -> int:
     return ((rows + 127) // 128) * 128 * (K // 16)
 
 
+def int4_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of an INT4-variant scale buffer: [rows][K/64] bf16."""
+    return rows * (K // 64) * 2
+
+
 def gelu_quant_scratch_bytes(M: int, N: int, rank2: int) -> int:
     """Scratch svdq_gemm_w4a4_gelu_quant needs (SVDQ_GELU_QUANT_SCRATCH_BYTES)."""
     return (128 + (M + 255) // 256) * 256 * rank2 * 4
@@ -142,6 +153,26 @@ def svdq_pack_weights(W: np.ndarray, x_absmax: np.ndarray, rank: int) -> dict:
     _check(st, "svdq_pack_weights")
     return {"N": N, "K": K, "rank": int(rank), "inv_lambda": inv, "L1s": L1s, "L2s": L2s,
             "w_codes": codes, "w_scales": scales, "w_tensor_scale": float(sT[0])}
+
+
+def svdq_pack_weights_int4(W: np.ndarray, x_absmax: np.ndarray, rank: int) -> dict:
+    """Offline packing, INT4 variant, of an nn.Linear weight W [N, K]
+    (float32).  Returns inv_lambda [K] fp32, L1s [rank, K] and L2 [N, rank]
+    bf16 bits, w_codes [N, K/2] and w_scales [N, K/64] bf16 bits."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    xm = np.ascontiguousarray(x_absmax, dtype=np.float32)
+    N, K = W.shape
+    r = max(int(rank), 0)
+    inv = np.zeros(K, dtype=np.float32)
+    L1s = np.zeros((r, K), dtype=np.uint16)
+    L2 = np.zeros((N, r), dtype=np.uint16)
+    codes = np.zeros((N, K // 2), dtype=np.uint8)
+    scales = np.zeros((N, K // 64), dtype=np.uint16)
+    st = _lib.svdq_pack_weights_int4(_np_ptr(W), N, K, _np_ptr(xm), int(rank), _np_ptr(inv),
+                                     _np_ptr(L1s), _np_ptr(L2), _np_ptr(codes), _np_ptr(scales))
+    _check(st, "svdq_pack_weights_int4")
+    return {"N": N, "K": K, "rank": int(rank), "inv_lambda": inv, "L1s": L1s, "L2": L2,
+            "w_codes": codes, "w_scales": scales}
 
 
 def awq_pack_weights(W: np.ndarray, group_size: int = 64):
@@ -227,6 +258,63 @@ def svdq_quantize_act(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None
                                 _dptr(dev_status), _stream_ptr(stream))
     _check(st, "svdq_quantize_act")
     return a_codes, a_scales, lora_act
+
+
+def svdq_quantize_act_int4(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales=None,
+                           lora_act=None, dev_status=None, stream=None):
+    """INT4 variant.  X: CUDA bf16 [M, K]; inv_lambda fp32 [K]; L1s bf16
+    bits [rank, K].  Returns (a_codes [M, K/2] uint8, a_scales [M, K/64]
+    bf16, lora_act [M, rank] bf16)."""
+    torch = _torch()
+    for t, n in ((X, "X"), (inv_lambda, "inv_lambda"), (L1s, "L1s"), (a_codes, "a_codes"),
+                 (a_scales, "a_scales"), (lora_act, "lora_act"), (dev_status, "dev_status")):
+        _check_cuda(t, n)
+    M, K = X.shape
+    dev = X.device
+    if a_codes is None:
+        a_codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    if a_scales is None:
+        a_scales = torch.empty((M, K // 64), dtype=torch.bfloat16, device=dev)
+    if lora_act is None:
+        lora_act = torch.empty((M, rank), dtype=torch.bfloat16, device=dev)
+    if M > 0:
+        for t, n, e, z in ((X, "X", M * K, 2), (inv_lambda, "inv_lambda", K, 4),
+                           (L1s, "L1s", rank * K, 2), (a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", M * (K // 64), 2),
+                           (lora_act, "lora_act", M * rank, 2), (dev_status, "dev_status", 1, 4)):
+            _need(t, n, e, z)
+    st = _lib.svdq_quantize_act_int4(_dptr(X), _dptr(inv_lambda), _dptr(L1s), M, K, int(rank),
+                                     _dptr(a_codes), _dptr(a_scales), _dptr(lora_act),
+                                     _dptr(dev_status), _stream_ptr(stream))
+    _check(st, "svdq_quantize_act_int4")
+    return a_codes, a_scales, lora_act
+
+
+def svdq_gemm_w4a4_int4(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias, M: int,
+                        N: int, K: int, rank: int, Y=None, stream=None):
+    """INT4 variant.  a_scales [M, K/64] and w_scales [N, K/64] bf16, L2
+    [N, rank] bf16.  Returns Y [M, N] bf16 (CUDA)."""
+    torch = _torch()
+    for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
+                 (w_scales, "w_scales"), (lora_act, "lora_act"), (L2, "L2"), (bias, "bias"),
+                 (Y, "Y")):
+        _check_cuda(t, n)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
+    if M > 0:
+        for t, n, e, z in ((a_codes, "a_codes", code_bytes(M, K), 1),
+                           (a_scales, "a_scales", M * (K // 64), 2),
+                           (w_codes, "w_codes", code_bytes(N, K), 1),
+                           (w_scales, "w_scales", N * (K // 64), 2),
+                           (lora_act, "lora_act", M * rank, 2), (L2, "L2", N * rank, 2),
+                           (bias, "bias", N, 2), (Y, "Y", M * N, 2)):
+            _need(t, n, e, z)
+    st = _lib.svdq_gemm_w4a4_int4(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes),
+                                  _dptr(w_scales), _dptr(lora_act), _dptr(L2), _dptr(bias),
+                                  _dptr(Y), int(M), int(N), int(K), int(rank),
+                                  _stream_ptr(stream))
+    _check(st, "svdq_gemm_w4a4_int4")
+    return Y
 
 
 def _gemm(name, a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, M,

@@ -17,10 +17,10 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsvdq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "awq_gemv.cu", "microbench.cu",
-                "selftest.cu"]
+CUDA_SOURCES = ["capi.cu", "quantize_act.cu", "gemm_w4a4.cu", "gemm_int4.cu", "awq_gemv.cu",
+                "microbench.cu", "selftest.cu"]
 HOST_SOURCES = ["pack.cpp"]
-HEADERS = ["device_common.cuh", "act_quant.cuh", "launch.h"]
+HEADERS = ["device_common.cuh", "act_quant.cuh", "int4_quant.cuh", "launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

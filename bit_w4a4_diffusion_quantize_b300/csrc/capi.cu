@@ -124,6 +124,33 @@ bool encode_rank_rows(CUtensorMap* map, const uint16_t* ptr, int rows, int rank,
                    (uint64_t)rank * 2, (uint32_t)rank, (uint32_t)box_rows, sw);
 }
 
+// svdq_quantize_act and its INT4 form: the same kernel, the quantization
+// step and the scale layout picked by `int4`
+svdq_status quantize_act_impl(const uint16_t* X_bf16, const float* inv_lambda,
+                              const uint16_t* L1s, int M, int K, int rank, uint8_t* a_codes,
+                              uint8_t* a_scales, uint16_t* lora_act, int* dev_status,
+                              void* stream, bool int4) {
+  if (M < 0 || K <= 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  if (M == 0) return SVDQ_OK;
+  if (!X_bf16 || !inv_lambda || !L1s || !a_codes || !a_scales || !lora_act) return SVDQ_ERR_NULL;
+  if (!aligned16(X_bf16) || !aligned16(inv_lambda) || !aligned16(L1s) || !aligned16(a_codes) ||
+      !aligned16(a_scales) || !aligned16(lora_act))
+    return SVDQ_ERR_ALIGN;
+  svdq_status st = current_device(nullptr, nullptr);
+  if (st != SVDQ_OK) return st;
+  CUtensorMap tm_x, tm_l1s;
+  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, X_bf16, (uint64_t)K, (uint64_t)M,
+                 (uint64_t)K * 2, 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_l1s, CU_TENSOR_MAP_DATA_TYPE_UINT16, L1s, (uint64_t)K, (uint64_t)rank,
+                 (uint64_t)K * 2, 64u, (uint32_t)rank, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SVDQ_ERR_CUDA;
+  cudaError_t e = svdq::launch_quantize_act(tm_x, tm_l1s, inv_lambda, M, K, rank, a_codes,
+                                            a_scales, lora_act, dev_status,
+                                            static_cast<cudaStream_t>(stream), int4);
+  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -151,25 +178,17 @@ svdq_status svdq_quantize_act(const uint16_t* X_bf16, const float* inv_lambda,
                               const uint16_t* L1s, int M, int K, int rank, uint8_t* a_codes,
                               uint8_t* a_scales, uint16_t* lora_act, int* dev_status,
                               void* stream) {
-  if (M < 0 || K <= 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
-  if (!rank_ok(rank)) return SVDQ_ERR_RANK;
-  if (M == 0) return SVDQ_OK;
-  if (!X_bf16 || !inv_lambda || !L1s || !a_codes || !a_scales || !lora_act) return SVDQ_ERR_NULL;
-  if (!aligned16(X_bf16) || !aligned16(inv_lambda) || !aligned16(L1s) || !aligned16(a_codes) ||
-      !aligned16(a_scales) || !aligned16(lora_act))
-    return SVDQ_ERR_ALIGN;
-  svdq_status st = current_device(nullptr, nullptr);
-  if (st != SVDQ_OK) return st;
-  CUtensorMap tm_x, tm_l1s;
-  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, X_bf16, (uint64_t)K, (uint64_t)M,
-                 (uint64_t)K * 2, 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_l1s, CU_TENSOR_MAP_DATA_TYPE_UINT16, L1s, (uint64_t)K, (uint64_t)rank,
-                 (uint64_t)K * 2, 64u, (uint32_t)rank, CU_TENSOR_MAP_SWIZZLE_128B))
-    return SVDQ_ERR_CUDA;
-  cudaError_t e = svdq::launch_quantize_act(tm_x, tm_l1s, inv_lambda, M, K, rank, a_codes,
-                                            a_scales, lora_act, dev_status,
-                                            static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+  return quantize_act_impl(X_bf16, inv_lambda, L1s, M, K, rank, a_codes, a_scales, lora_act,
+                           dev_status, stream, false);
+}
+
+svdq_status svdq_quantize_act_int4(const uint16_t* X_bf16, const float* inv_lambda,
+                                   const uint16_t* L1s, int M, int K, int rank, uint8_t* a_codes,
+                                   uint16_t* a_scales, uint16_t* lora_act, int* dev_status,
+                                   void* stream) {
+  return quantize_act_impl(X_bf16, inv_lambda, L1s, M, K, rank, a_codes,
+                           reinterpret_cast<uint8_t*>(a_scales), lora_act, dev_status, stream,
+                           true);
 }
 
 }  // extern "C"
@@ -303,6 +322,27 @@ svdq_status svdq_gemm_w4a4_gelu_quant(const uint8_t* a_codes, const uint8_t* a_s
   return gemm_w4a4(a_codes, a_scales, w_codes, w_scales, w_tensor_scale, lora_act, L2s, bias, H,
                    M, N, K, rank, svdq::GemmEpilogue::kGeluQuant, svdq::QkvEpilogue{}, gq, L1s2,
                    dev_status, stream);
+}
+
+svdq_status svdq_gemm_w4a4_int4(const uint8_t* a_codes, const uint16_t* a_scales,
+                                const uint8_t* w_codes, const uint16_t* w_scales,
+                                const uint16_t* lora_act, const uint16_t* L2,
+                                const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
+                                void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (!rank_ok(rank)) return SVDQ_ERR_RANK;
+  if (M == 0) return SVDQ_OK;
+  if (!a_codes || !a_scales || !w_codes || !w_scales || !lora_act || !L2 || !Y)
+    return SVDQ_ERR_NULL;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) ||
+      !aligned16(w_scales) || !aligned16(lora_act) || !aligned16(L2) || !aligned16(Y) ||
+      (bias && !aligned16(bias)))
+    return SVDQ_ERR_ALIGN;
+  svdq_status st = current_device(nullptr, nullptr);
+  if (st != SVDQ_OK) return st;
+  cudaError_t e = svdq::launch_gemm_int4(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias,
+                                         Y, M, N, K, rank, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 
 svdq_status awq_gemv_w4a16(const uint16_t* X_bf16, const uint8_t* qweight,

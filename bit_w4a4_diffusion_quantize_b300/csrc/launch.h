@@ -13,7 +13,13 @@ namespace svdq {
 cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s,
                                 const float* inv_lambda, int M, int K, int rank,
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
-                                int* dev_status, cudaStream_t stream);
+                                int* dev_status, cudaStream_t stream, bool int4);
+
+// INT4 variant's GEMM (gemm_int4.cu): grid N/128 x ceil(M/128)
+cudaError_t launch_gemm_int4(const uint8_t* a_codes, const uint16_t* a_scales,
+                             const uint8_t* w_codes, const uint16_t* w_scales,
+                             const uint16_t* lora_act, const uint16_t* L2, const uint16_t* bias,
+                             uint16_t* Y, int M, int N, int K, int rank, cudaStream_t stream);
 
 // Tensor maps of svdq_gemm_w4a4 (and of its GELU and QKV variants).  The
 // kernel runs on CTA pairs: each CTA loads its own 128 A rows and one half

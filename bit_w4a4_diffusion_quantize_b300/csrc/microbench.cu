@@ -13,6 +13,10 @@
 // mode 5: mode 0 with consecutive MMAs alternating between two accumulators
 //         (n = 128: columns 0 and 128)
 // mode 6: mode 3 with the same alternation (n = 128)
+// mode 7: the legacy warp-level MMA of the INT4 variant's GEMM, mma.sync
+//         m16n8k32 e4m3 with fp32 accumulation (n = 128): 8 warps per CTA,
+//         each issuing 16 independent MMAs per iteration, operands in
+//         registers
 #include <cstdint>
 
 #include "../../include/svdq_bench.h"
@@ -141,13 +145,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// mode 7: 8 warps x 16 accumulators; 128 m16n8k32 MMAs per CTA and iteration
+// (2 * 16 * 8 * 32 * 128 = 2 * 128 * 128 * 32 flops, the formula with n = 128,
+// K_mma = 32).  Operands: e4m3 1.0 (0x38) and 2.0 (0x40).  The accumulators
+// feed a store under a condition the compiler cannot decide (iters < 0; the
+// host rejects it), so that no MMA is dead code.
+__global__ void __launch_bounds__(256, 1) k_mma_rate_warp(int iters, int* dev_status) {
+  const uint32_t a0 = 0x38403840u, a1 = 0x40383840u, a2 = 0x38384040u, a3 = 0x40404038u,
+                 b0 = 0x38383838u, b1 = 0x40384038u;
+  float d[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d[j][c] = 0.0f;
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, "
+          "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(d[j][0]), "+f"(d[j][1]), "+f"(d[j][2]), "+f"(d[j][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) s += d[j][0] + d[j][1] + d[j][2] + d[j][3];
+  if (iters < 0 && dev_status) *dev_status = (int)s;
+}
+
 }  // namespace
 }  // namespace svdq
 
 extern "C" svdq_status svdq_bench_mma_rate(int mode, int n, int iters, int ctas,
                                            int* dev_status, void* stream) {
-  if (mode < 0 || mode > 6 || (n != 128 && n != 256) || iters < 1 || ctas < 1)
+  if (mode < 0 || mode > 7 || (n != 128 && n != 256) || iters < 1 || ctas < 1)
     return SVDQ_ERR_SHAPE;
+  if (mode == 7 && n != 128) return SVDQ_ERR_SHAPE;
   const bool pair = mode == 3 || mode == 4 || mode == 6;
   if (pair && ctas % 2 != 0) return SVDQ_ERR_SHAPE;  // whole CTA pairs
   if (mode >= 5 && n != 128) return SVDQ_ERR_SHAPE;  // two accumulators of 128 columns
@@ -159,6 +192,11 @@ extern "C" svdq_status svdq_bench_mma_rate(int mode, int n, int iters, int ctas,
     return SVDQ_ERR_CUDA;
   }
   if (major != 10 || minor != 3) return SVDQ_ERR_UNSUPPORTED_ARCH;
+  if (mode == 7) {
+    svdq::k_mma_rate_warp<<<ctas, 256, 0, static_cast<cudaStream_t>(stream)>>>(iters,
+                                                                              dev_status);
+    return cudaGetLastError() == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
+  }
   const int smem = 16384 + 32768 + 4096 + 64 + 1024;
   if (pair) {
     if (cudaFuncSetAttribute(svdq::k_mma_rate_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,

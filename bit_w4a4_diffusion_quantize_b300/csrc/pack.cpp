@@ -393,6 +393,77 @@ bool all_finite(const float* p, size_t n) {
   return true;
 }
 
+// Round-to-nearest for the scope of a packing call (the caller's mode is
+// put back on every return path).
+struct RoundingScope {
+  int saved = std::fegetround();
+  RoundingScope() { std::fesetround(FE_TONEAREST); }
+  ~RoundingScope() { std::fesetround(saved); }
+};
+
+// Steps shared by the NVFP4 and INT4 packers: (1) smoothing, inv_lambda;
+// (2) the rank-r factors of W_hat^T, L1s = bf16(inv (.) L1) written to L1s
+// [rank][K] and bf16(L2) returned as doubles l2d [rank][N]; (3) the residual
+// R[n][k] = (W[n][k] - sum_i L1s[i][k] L2[i][n]) / inv[k] (sum over i
+// ascending) returned in A [N][K].  False if the smoothing is not finite.
+bool factor_and_residual(const float* W, int N, int K, const float* x_absmax, int rank,
+                         float* inv_lambda, uint16_t* L1s, std::vector<double>& A,
+                         std::vector<double>& l2d) {
+  const int64_t NN = N, KK = K;
+  // (1) smoothing: lambda_j = sqrt(max|X_j| / max|W_j|), clamped
+  std::vector<double> inv(K);
+  for (int k = 0; k < K; ++k) {
+    double wm = 0.0;
+    for (int n = 0; n < N; ++n) wm = std::max(wm, (double)std::fabs(W[(size_t)n * K + k]));
+    const double xm = (double)x_absmax[k];
+    double lam = 1.0;
+    if (xm > 0.0 && wm > 0.0) lam = std::sqrt(xm / wm);
+    lam = std::min(std::max(lam, std::ldexp(1.0, -20)), std::ldexp(1.0, 20));
+    inv_lambda[k] = (float)(1.0 / lam);
+    inv[k] = (double)inv_lambda[k];
+    if (!std::isfinite(inv[k])) return false;
+  }
+  // (2) W_hat = W diag(1/inv_lambda) (N x K); its transpose is the K x N
+  // matrix the method factors
+  A.assign((size_t)NN * KK, 0.0);
+  parallel_for(NN, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n)
+      for (int64_t k = 0; k < KK; ++k)
+        A[(size_t)n * KK + k] = (double)W[(size_t)n * KK + k] / inv[k];
+  });
+  Thin U, Vk;
+  std::vector<double> sig;
+  truncated_svd(A, NN, KK, rank, U, sig, Vk);
+  // W_hat^T ~= Vk S U^T  ->  L1 = Vk S (K x r), L2 = U^T (r x N)
+  std::vector<uint16_t> l1s((size_t)rank * K), l2((size_t)rank * N);
+  for (int i = 0; i < rank; ++i) {
+    for (int k = 0; k < K; ++k)
+      l1s[(size_t)i * K + k] = bf16_from_double(inv[k] * (Vk.col(i)[k] * sig[i]));
+    for (int n = 0; n < N; ++n) l2[(size_t)i * N + n] = bf16_from_double(U.col(i)[n]);
+  }
+  std::memcpy(L1s, l1s.data(), l1s.size() * sizeof(uint16_t));
+  std::vector<double> l1d((size_t)rank * K);
+  l2d.assign((size_t)rank * N, 0.0);
+  for (size_t i = 0; i < l1d.size(); ++i) l1d[i] = bf16_to_double(l1s[i]);
+  for (size_t i = 0; i < l2d.size(); ++i) l2d[i] = bf16_to_double(l2[i]);
+  // (3) residual, stored over A
+  parallel_for(NN, [&](int64_t b, int64_t e) {
+    std::vector<double> acc(KK);
+    for (int64_t n = b; n < e; ++n) {
+      std::fill(acc.begin(), acc.end(), 0.0);
+      for (int i = 0; i < rank; ++i) {
+        const double c = l2d[(size_t)i * N + n];
+        const double* l1 = l1d.data() + (size_t)i * K;
+        for (int64_t k = 0; k < KK; ++k) acc[k] += l1[k] * c;
+      }
+      double* rrow = A.data() + (size_t)n * KK;
+      for (int64_t k = 0; k < KK; ++k)
+        rrow[k] = ((double)W[(size_t)n * KK + k] - acc[k]) / inv[k];
+    }
+  });
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -421,66 +492,15 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
   if (!all_finite(W, (size_t)N * K) || !all_finite(x_absmax, (size_t)K)) return SVDQ_ERR_VALUE;
   for (int k = 0; k < K; ++k)
     if (x_absmax[k] < 0.0f) return SVDQ_ERR_VALUE;
-  const int saved_round = std::fegetround();
-  std::fesetround(FE_TONEAREST);
+  RoundingScope rounding;
   try {
     const int64_t NN = N, KK = K;
-    // (1) smoothing: lambda_j = sqrt(max|X_j| / max|W_j|), clamped
-    std::vector<double> inv(K);
-    for (int k = 0; k < K; ++k) {
-      double wm = 0.0;
-      for (int n = 0; n < N; ++n) wm = std::max(wm, (double)std::fabs(W[(size_t)n * K + k]));
-      const double xm = (double)x_absmax[k];
-      double lam = 1.0;
-      if (xm > 0.0 && wm > 0.0) lam = std::sqrt(xm / wm);
-      lam = std::min(std::max(lam, std::ldexp(1.0, -20)), std::ldexp(1.0, 20));
-      inv_lambda[k] = (float)(1.0 / lam);
-      inv[k] = (double)inv_lambda[k];
-    }
-    // (2) W_hat = W diag(1/inv_lambda) (N x K); its transpose is the K x N
-    // matrix the method factors
-    std::vector<double> A((size_t)NN * KK);
-    parallel_for(NN, [&](int64_t b, int64_t e) {
-      for (int64_t n = b; n < e; ++n)
-        for (int64_t k = 0; k < KK; ++k)
-          A[(size_t)n * KK + k] = (double)W[(size_t)n * KK + k] / inv[k];
-    });
-    Thin U, Vk;
-    std::vector<double> sig;
-    truncated_svd(A, NN, KK, rank, U, sig, Vk);
-    // W_hat^T ~= Vk S U^T  ->  L1 = Vk S (K x r), L2 = U^T (r x N)
-    std::vector<uint16_t> l1s((size_t)rank * K), l2((size_t)rank * N);
-    for (int i = 0; i < rank; ++i) {
-      for (int k = 0; k < K; ++k)
-        l1s[(size_t)i * K + k] = bf16_from_double(inv[k] * (Vk.col(i)[k] * sig[i]));
-      for (int n = 0; n < N; ++n) l2[(size_t)i * N + n] = bf16_from_double(U.col(i)[n]);
-    }
-    std::memcpy(L1s, l1s.data(), l1s.size() * sizeof(uint16_t));
-    std::vector<double> l1d((size_t)rank * K), l2d((size_t)rank * N);
-    for (size_t i = 0; i < l1d.size(); ++i) l1d[i] = bf16_to_double(l1s[i]);
-    for (size_t i = 0; i < l2d.size(); ++i) l2d[i] = bf16_to_double(l2[i]);
-    // (3) residual R[n][k] = (W[n][k] - sum_i L1s[i][k] L2[i][n]) / inv[k],
-    // stored over A; sum over i ascending
-    parallel_for(NN, [&](int64_t b, int64_t e) {
-      std::vector<double> acc(KK);
-      for (int64_t n = b; n < e; ++n) {
-        std::fill(acc.begin(), acc.end(), 0.0);
-        for (int i = 0; i < rank; ++i) {
-          const double c = l2d[(size_t)i * N + n];
-          const double* l1 = l1d.data() + (size_t)i * K;
-          for (int64_t k = 0; k < KK; ++k) acc[k] += l1[k] * c;
-        }
-        double* rrow = A.data() + (size_t)n * KK;
-        for (int64_t k = 0; k < KK; ++k)
-          rrow[k] = ((double)W[(size_t)n * KK + k] - acc[k]) / inv[k];
-      }
-    });
+    std::vector<double> A, l2d;
+    if (!factor_and_residual(W, N, K, x_absmax, rank, inv_lambda, L1s, A, l2d))
+      return SVDQ_ERR_VALUE;
     double amax = 0.0;
     for (size_t i = 0; i < A.size(); ++i) amax = std::max(amax, std::fabs(A[i]));
-    if (!std::isfinite(amax)) {
-      std::fesetround(saved_round);
-      return SVDQ_ERR_VALUE;
-    }
+    if (!std::isfinite(amax)) return SVDQ_ERR_VALUE;
     // (4) tensor scale: smallest power of two p with 6*448*p >= max|R|
     double sT = 1.0;
     if (amax > 0.0) {
@@ -490,10 +510,7 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
       while (bound * std::ldexp(1.0, e - 1) >= amax) --e;
       sT = std::ldexp(1.0, e);
     }
-    if (sT < std::ldexp(1.0, -100) || sT > std::ldexp(1.0, 100)) {
-      std::fesetround(saved_round);
-      return SVDQ_ERR_VALUE;
-    }
+    if (sT < std::ldexp(1.0, -100) || sT > std::ldexp(1.0, 100)) return SVDQ_ERR_VALUE;
     *w_tensor_scale = (float)sT;
     // L2s[n][i] = bf16(L2)[i][n] / s_T: exact, s_T is a power of two
     for (int n = 0; n < N; ++n)
@@ -524,10 +541,59 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
       }
     });
   } catch (const std::bad_alloc&) {
-    std::fesetround(saved_round);
     return SVDQ_ERR_NOMEM;
   }
-  std::fesetround(saved_round);
+  return SVDQ_OK;
+}
+
+svdq_status svdq_pack_weights_int4(const float* W, int N, int K, const float* x_absmax, int rank,
+                                   float* inv_lambda, uint16_t* L1s, uint16_t* L2,
+                                   uint8_t* w_codes, uint16_t* w_scales) {
+  if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
+  if (rank < 1 || rank > std::min(N, K)) return SVDQ_ERR_RANK;
+  if (!W || !x_absmax || !inv_lambda || !L1s || !L2 || !w_codes || !w_scales)
+    return SVDQ_ERR_NULL;
+  if (!all_finite(W, (size_t)N * K) || !all_finite(x_absmax, (size_t)K)) return SVDQ_ERR_VALUE;
+  for (int k = 0; k < K; ++k)
+    if (x_absmax[k] < 0.0f) return SVDQ_ERR_VALUE;
+  RoundingScope rounding;
+  try {
+    const int64_t NN = N, KK = K;
+    std::vector<double> A, l2d;
+    if (!factor_and_residual(W, N, K, x_absmax, rank, inv_lambda, L1s, A, l2d))
+      return SVDQ_ERR_VALUE;
+    for (size_t i = 0; i < A.size(); ++i)
+      if (!std::isfinite(A[i])) return SVDQ_ERR_VALUE;
+    for (int n = 0; n < N; ++n)
+      for (int i = 0; i < rank; ++i)
+        L2[(size_t)n * rank + i] = bf16_from_double(l2d[(size_t)i * N + n]);
+    // symmetric groups of 64 consecutive k of one output channel:
+    // s = bf16(amax / 7), q = clamp(RNE(R / s), -8, 7), a zero scale gives 0
+    const size_t G = (size_t)K / 64;
+    parallel_for(NN, [&](int64_t b, int64_t e) {
+      for (int64_t n = b; n < e; ++n) {
+        const double* rrow = A.data() + (size_t)n * KK;
+        for (size_t g = 0; g < G; ++g) {
+          const double* grp = rrow + g * 64;
+          double gmax = 0.0;
+          for (int i = 0; i < 64; ++i) gmax = std::max(gmax, std::fabs(grp[i]));
+          const uint16_t sbits = bf16_from_double(gmax / 7.0);
+          w_scales[(size_t)n * G + g] = sbits;
+          const double s = bf16_to_double(sbits);
+          uint8_t* out = w_codes + (size_t)n * (KK / 2) + g * 32;
+          for (int i = 0; i < 32; ++i) {
+            int q[2] = {0, 0};
+            for (int h = 0; h < 2; ++h)
+              if (s > 0.0)
+                q[h] = (int)std::min(7.0, std::max(-8.0, std::nearbyint(grp[2 * i + h] / s)));
+            out[i] = (uint8_t)((q[0] & 0xF) | ((q[1] & 0xF) << 4));
+          }
+        }
+      }
+    });
+  } catch (const std::bad_alloc&) {
+    return SVDQ_ERR_NOMEM;
+  }
   return SVDQ_OK;
 }
 

@@ -39,6 +39,7 @@
 
 #include "act_quant.cuh"
 #include "device_common.cuh"
+#include "int4_quant.cuh"
 #include "launch.h"
 
 namespace svdq {
@@ -106,7 +107,9 @@ __device__ unsigned long long* g_quant_trace = nullptr;
   } while (0)
 #endif
 
-template <int RANK>
+// INT4: the INT4 variant's quantization (64-element groups over the quad,
+// bf16 scales [M][K/64] row-major); the rest of the kernel is shared.
+template <int RANK, bool INT4>
 __global__ void __launch_bounds__(kThreads, 1)
     k_quantize_act(const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_l1s, const float* __restrict__ inv_lambda,
@@ -223,10 +226,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- quantization: one block per row
     uint2 ca, cb;
     uint32_t sa, sb;
-    quant_block16(xa, inv, r6, tab, ca, sa);
-    quant_block16(xb, inv, r6, tab, cb, sb);
+    if constexpr (INT4) {
+      quant_group64_int4(xa, inv, ca, sa);
+      quant_group64_int4(xb, inv, cb, sb);
+    } else {
+      quant_block16(xa, inv, r6, tab, ca, sa);
+      quant_block16(xb, inv, r6, tab, cb, sb);
+    }
     if (rowA < M) *reinterpret_cast<uint2*>(a_codes + (size_t)rowA * (K >> 1) + (k0 >> 1)) = ca;
     if (rowB < M) *reinterpret_cast<uint2*>(a_codes + (size_t)rowB * (K >> 1) + (k0 >> 1)) = cb;
+    if constexpr (INT4) {
+      // the row's 64-group scale (every lane of the quad holds it): lane
+      // t = 0 writes row g's, lane t = 1 row g+8's
+      if (t < 2) {
+        const int r = t == 0 ? rowA : rowB;
+        if (r < M)
+          reinterpret_cast<uint16_t*>(a_scales)[(size_t)r * (K >> 6) + step] =
+              (uint16_t)(t == 0 ? sa : sb);
+      }
+      if (lane == 0 && warp == 0) SVDQ_QTR(32, i);
+      if (lane == 0 && warp == kWarps - 1) SVDQ_QTR(64, i);
+      continue;
+    }
     // gather the 4 scale bytes of each row's 64-wide step across the quad;
     // lane t = 0 writes row g's word, lane t = 1 row g+8's (tile layout:
     // tile (r/128, c/4) of 512 bytes; entry (r%32)*16 + ((r/32)%4)*4 + c%4)
@@ -276,12 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int RANK>
+template <int RANK, bool INT4>
 cudaError_t launch_t(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s, const float* inv_lambda,
                      int M, int K, uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
                      int* dev_status, cudaStream_t stream) {
   using C = QCfg<RANK>;
-  auto kern = k_quantize_act<RANK>;
+  auto kern = k_quantize_act<RANK, INT4>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -306,20 +327,21 @@ cudaError_t launch_t(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s, const f
 cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l1s,
                                 const float* inv_lambda, int M, int K, int rank,
                                 uint8_t* a_codes, uint8_t* a_scales, uint16_t* lora_act,
-                                int* dev_status, cudaStream_t stream) {
+                                int* dev_status, cudaStream_t stream, bool int4) {
+#define SVDQ_QA_CASE(R_)                                                                  \
+  case R_:                                                                                \
+    return int4 ? launch_t<R_, true>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales,  \
+                                     lora_act, dev_status, stream)                        \
+                : launch_t<R_, false>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, \
+                                      lora_act, dev_status, stream);
   switch (rank) {
-    case 16:
-      return launch_t<16>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
-                          dev_status, stream);
-    case 32:
-      return launch_t<32>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
-                          dev_status, stream);
-    case 64:
-      return launch_t<64>(tm_x, tm_l1s, inv_lambda, M, K, a_codes, a_scales, lora_act,
-                          dev_status, stream);
+    SVDQ_QA_CASE(16)
+    SVDQ_QA_CASE(32)
+    SVDQ_QA_CASE(64)
     default:
       return cudaErrorInvalidValue;
   }
+#undef SVDQ_QA_CASE
 }
 
 }  // namespace svdq

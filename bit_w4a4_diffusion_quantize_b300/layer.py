@@ -1,4 +1,5 @@
-"""Layer-level wrappers: a packed SVDQ W4A4 linear and an AWQ W4A16 linear
+"""Layer-level wrappers: a packed SVDQ W4A4 linear (NVFP4, or the INT4
+variant) and an AWQ W4A16 linear
 holding their device buffers.  ``forward`` is the per-call path a user runs
 (two library calls for SVDQ: svdq_quantize_act then svdq_gemm_w4a4; one for
 AWQ).  Pure marshalling: buffers are torch tensors, all arithmetic is in
@@ -52,6 +53,46 @@ class SVDQLinear:
         return gemm(a_codes, a_scales, self.w_codes, self.w_scales, self.w_tensor_scale, lora,
                     self.L2s, self.bias, M, self.N, self.K, self.rank, out,
                     dev_status=dev_status, stream=stream)
+
+    __call__ = forward
+
+
+class SVDQLinearInt4:
+    """The INT4 variant: Y = svdq_gemm_w4a4_int4(svdq_quantize_act_int4(X))
+    for a weight packed once by svdq_pack_weights_int4."""
+
+    def __init__(self, packed: dict, bias_bf16_bits=None, device="cuda"):
+        import torch
+
+        self.N, self.K, self.rank = packed["N"], packed["K"], packed["rank"]
+        dev = torch.device(device)
+
+        def t(a, dtype):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dtype)
+
+        def bf16(a):
+            return t(np.asarray(a, dtype=np.uint16).view(np.int16), torch.bfloat16)
+
+        self.inv_lambda = t(packed["inv_lambda"].astype(np.float32), torch.float32)
+        self.L1s, self.L2 = bf16(packed["L1s"]), bf16(packed["L2"])
+        self.w_codes = t(packed["w_codes"].astype(np.uint8), torch.uint8)
+        self.w_scales = bf16(packed["w_scales"])
+        self.bias = None if bias_bf16_bits is None else bf16(bias_bf16_bits)
+
+    @classmethod
+    def from_float(cls, W: np.ndarray, x_absmax: np.ndarray, rank: int, bias_bf16_bits=None,
+                   device="cuda"):
+        return cls(_lib.svdq_pack_weights_int4(W, x_absmax, rank), bias_bf16_bits, device)
+
+    def forward(self, X, out=None, act_buffers=None, dev_status=None, stream=None):
+        M = X.shape[0]
+        bufs = act_buffers or (None, None, None)
+        a_codes, a_scales, lora = _lib.svdq_quantize_act_int4(
+            X, self.inv_lambda, self.L1s, self.rank, *bufs, dev_status=dev_status,
+            stream=stream)
+        return _lib.svdq_gemm_w4a4_int4(a_codes, a_scales, self.w_codes, self.w_scales, lora,
+                                        self.L2, self.bias, M, self.N, self.K, self.rank, out,
+                                        stream=stream)
 
     __call__ = forward
 

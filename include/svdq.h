@@ -173,6 +173,31 @@ svdq_status svdq_pack_weights(const float* W, int N, int K, const float* x_absma
 svdq_status awq_pack_weights(const float* W, int N, int K, int group_size,
                              uint8_t* qweight, uint16_t* scales, uint16_t* zeros);
 
+/* INT4 variant of the SVDQ W4A4 layer (dothoosh.com, "How Nunchaku Lite
+ * halves the VRAM of diffusion models", kernel-family list: svdq_w4a4 in INT4
+ * and NVFP4 variants; hardware list: INT4 is the pre-Blackwell format; the
+ * config block's int4 group size, 64).  4-bit values are signed integers
+ * -8..7 (two's complement nibbles, same byte order as the NVFP4 codes) with
+ * one bf16 scale per 64 consecutive k, row-major [rows][K/64]:
+ *   s = RNE_bf16(amax64 / 7),  q = clamp(RNE(v / s), -8, 7),
+ *   a group whose scale is 0 (or, for activations, not finite) has codes 0.
+ * SVDQ_INT4_SCALE_BYTES(rows, K) is the size of a scale buffer. */
+#define SVDQ_INT4_SCALE_BYTES(rows, K) ((size_t)(rows) * ((size_t)(K) / 64) * 2)
+
+/* Offline packing, INT4 variant: smoothing, low-rank factors and residual R
+ * exactly as svdq_pack_weights, then per output channel and 64-group of R:
+ *   w_scales = bf16(amax / 7) (float64 quotient),  w_codes = clamp(RNE(R /
+ *   s), -8, 7) (float64 quotient, ties to even).
+ * No tensor scale: L2 is bf16(L2) transposed, [N][rank].
+ * Sizes: N % 128 == 0, K % 128 == 0, 1 <= rank <= min(K, N).  Buffers:
+ * inv_lambda [K], L1s [rank*K], L2 [N*rank], w_codes SVDQ_CODE_BYTES(N, K),
+ * w_scales SVDQ_INT4_SCALE_BYTES(N, K) (bf16 bit patterns).
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_VALUE
+ * (non-finite W, x_absmax or residual), SVDQ_ERR_NOMEM. */
+svdq_status svdq_pack_weights_int4(const float* W, int N, int K, const float* x_absmax,
+                                   int rank, float* inv_lambda, uint16_t* L1s,
+                                   uint16_t* L2, uint8_t* w_codes, uint16_t* w_scales);
+
 /* ---------------------------------------------------------------- device */
 
 /* Activation side of the SVDQ linear, one kernel (fused-kernel paragraph:
@@ -336,6 +361,42 @@ svdq_status svdq_gemm_w4a4_qkv(const uint8_t* a_codes, const uint8_t* a_scales,
                                const float* rope_cos, const float* rope_sin, float eps,
                                uint16_t* QKV, int M, int N, int K, int rank, int* dev_status,
                                void* stream);
+
+/* Activation side of the INT4 variant, one kernel (the same fused pass as
+ * svdq_quantize_act: lora_act = bf16(X . L1s) alongside the codes):
+ *   x_hat    = fl32(X[m][k] * inv_lambda[k])
+ *   a_scales = RNE_bf16( fl32(amax64(x_hat) / 7) )   [M][K/64] bf16 bits
+ *   a_codes  = clamp(RNE(x_hat / s), -8, 7)          [M][K/2] packed,
+ *              rounded from the exact quotient; codes 0 where s is 0 or inf
+ * Inputs, sizes, lora_act and errors as svdq_quantize_act (K % 128 == 0, rank
+ * in {16, 32, 64}).  Output buffers: a_codes SVDQ_CODE_BYTES(M, K), a_scales
+ * SVDQ_INT4_SCALE_BYTES(M, K), lora_act [M][rank]. */
+svdq_status svdq_quantize_act_int4(const uint16_t* X_bf16, const float* inv_lambda,
+                                   const uint16_t* L1s, int M, int K, int rank,
+                                   uint8_t* a_codes, uint16_t* a_scales, uint16_t* lora_act,
+                                   int* dev_status, void* stream);
+
+/* The 4-bit GEMM of the INT4 variant with the low-rank up projection and the
+ * bias (the fused-kernel paragraph's second kernel):
+ *   Y[m][n] = bf16( sum_g a_s[m][g] w_s[n][g] sum_{k in g} a_q[m][k] w_q[n][k]
+ *                   + sum_i lora_act[m][i] L2[n][i] + bias[n] )
+ * fp32 accumulation: each group's integer sum is exact, then added with one
+ * fma by the (exact) product of its two scales; one rounding to bf16.  B300
+ * has no 4-bit integer tensor-core path: the codes run on the warp-level FP8
+ * MMA (every code is an exact e4m3 value).
+ * Inputs: a_codes [M][K/2], a_scales [M][K/64] bf16 (svdq_quantize_act_int4),
+ * w_codes [N][K/2], w_scales [N][K/64] bf16, L2 [N][rank] bf16
+ * (svdq_pack_weights_int4), lora_act [M][rank] bf16, bias [N] bf16 or NULL.
+ * Output: Y [M][N] bf16.
+ * Sizes: M >= 0 (M == 0 launches nothing), N % 128 == 0, K % 128 == 0, rank in
+ * {16, 32, 64}.
+ * Errors: SVDQ_ERR_NULL, SVDQ_ERR_SHAPE, SVDQ_ERR_RANK, SVDQ_ERR_ALIGN,
+ * SVDQ_ERR_UNSUPPORTED_ARCH, SVDQ_ERR_CUDA. */
+svdq_status svdq_gemm_w4a4_int4(const uint8_t* a_codes, const uint16_t* a_scales,
+                                const uint8_t* w_codes, const uint16_t* w_scales,
+                                const uint16_t* lora_act, const uint16_t* L2,
+                                const uint16_t* bias, uint16_t* Y, int M, int N, int K,
+                                int rank, void* stream);
 
 /* AWQ W4A16 GEMV for the small-M modulation layers (kernel-family list:
  * memory-bound adaLN modulation):

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import workloads
-from oracle import awq, formats, layout, svdq
+from oracle import awq, formats, int4, layout, svdq
 
 import bit_w4a4_diffusion_quantize_b300 as lib
 
@@ -38,7 +38,8 @@ def test_library_exports_every_declared_symbol():
     assert {"svdq_pack_weights", "svdq_quantize_act", "svdq_gemm_w4a4", "svdq_gemm_w4a4_gelu",
             "svdq_gemm_w4a4_qkv", "svdq_gemm_w4a4_gelu_quant", "awq_gemv_w4a16",
             "awq_pack_weights", "svdq_calib_absmax", "svdq_check_device",
-            "svdq_status_string"} <= names
+            "svdq_status_string", "svdq_pack_weights_int4", "svdq_quantize_act_int4",
+            "svdq_gemm_w4a4_int4"} <= names
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
@@ -168,6 +169,25 @@ def test_gelu_quant_static_argument_errors():
     assert call(M=0) == 0
 
 
+def _qa4(X=ALIGNED, M=64, K=256, r=32, sc=ALIGNED, lora=ALIGNED):
+    return lib.raw_lib().svdq_quantize_act_int4(X, ALIGNED, ALIGNED, M, K, r, ALIGNED, sc, lora,
+                                                None, None)
+
+
+def _g4(M=64, N=256, K=256, r=32, Y=ALIGNED, a=ALIGNED, sw=ALIGNED, bias=None):
+    return lib.raw_lib().svdq_gemm_w4a4_int4(a, ALIGNED, ALIGNED, sw, ALIGNED, ALIGNED, bias, Y,
+                                             M, N, K, r, None)
+
+
+def test_int4_argument_errors():
+    assert _qa4(K=192) == -2 and _qa4(M=-1) == -2 and _qa4(r=8) == -6
+    assert _qa4(X=P(0)) == -1 and _qa4(sc=MISALIGNED) == -3 and _qa4(M=0, X=P(0)) == 0
+    assert _g4(N=192) == -2 and _g4(K=64) == -2 and _g4(M=-1) == -2 and _g4(r=48) == -6
+    assert _g4(Y=P(0)) == -1 and _g4(sw=P(0)) == -1
+    assert _g4(a=MISALIGNED) == -3 and _g4(bias=MISALIGNED) == -3
+    assert _g4(M=0, Y=P(0)) == 0
+
+
 def test_awq_argument_errors():
     assert _awq(M=0) == -2 and _awq(M=9) == -2 and _awq(g=128) == -2
     assert _awq(N=0) == -2 and _awq(N=12) == -2 and _awq(K=4224) == -2
@@ -178,6 +198,7 @@ def test_awq_argument_errors():
 @pytest.mark.skipif(HAS_GPU, reason="valid arguments would launch on a real device")
 def test_device_calls_without_device_report_cuda_error():
     assert _qa() == -5 and _gemm() == -5 and _awq() == -5
+    assert _qa4() == -5 and _g4() == -5
     assert _gemm(fn="svdq_gemm_w4a4_gelu") == -5 and _qkv() == -5 and _gq() == -5
     assert _gq(H=ALIGNED) == -5
 
@@ -233,6 +254,42 @@ def test_packer_full_rank_leaves_rounding_residual():
     R = svdq.residual(W, p["inv_lambda"], L1s, L2)
     # only the bf16 rounding of the factors is left
     assert np.linalg.norm(R) <= 2.0 ** -7 * np.linalg.norm(W_hat)
+
+
+@pytest.mark.parametrize("case", [
+    workloads.CASES["tiny"],                                 # direct Jacobi SVD path
+    workloads.custom_case(256, 512, 384, 32, seed=3),        # randomized subspace path
+], ids=lambda c: f"{c.name}-{c.N}x{c.K}-r{c.rank}")
+def test_int4_packer_matches_oracle(case):
+    """svdq_pack_weights_int4: the same smoothing as the oracle; codes and
+    scales equal to the oracle's INT4 quantization of the residual of the
+    packer's own factors; the factors those of the NVFP4 packer (same
+    steps); the residual near the LAPACK-optimal one."""
+    X = workloads.make_activations(case)
+    W, b = workloads.make_weights(case)
+    xm = svdq.calib_absmax(X)
+    p = lib.svdq_pack_weights_int4(W, xm, case.rank)
+    assert np.array_equal(p["inv_lambda"], svdq.smoothing_inv_lambda(xm, W))
+    L1s = formats.bf16_from_bits(p["L1s"]).T
+    L2 = formats.bf16_from_bits(p["L2"]).T
+    R = svdq.residual(W, p["inv_lambda"], L1s, L2)
+    codes, scales = int4.quantize_weight_residual(R)
+    assert np.array_equal(p["w_codes"], int4.pack_codes(codes))
+    assert np.array_equal(p["w_scales"], formats.bf16_bits(scales))
+    q = lib.svdq_pack_weights(W, xm, case.rank)
+    assert np.array_equal(p["L1s"], q["L1s"])
+    ref = int4.pack_weights(W, xm, case.rank)
+    assert np.linalg.norm(R) <= 1.01 * np.linalg.norm(ref["R"])
+
+
+def test_int4_packer_argument_errors():
+    W = np.zeros((128, 128), np.float32)
+    xm = np.ones(128, np.float32)
+    for args, st in (((np.zeros((100, 128), np.float32), xm, 16), -2), ((W, xm, 0), -6),
+                     ((np.full((128, 128), np.nan, np.float32), xm, 16), -7)):
+        with pytest.raises(lib.SvdqError) as e:
+            lib.svdq_pack_weights_int4(*args)
+        assert e.value.status == st
 
 
 def test_packer_argument_errors():
