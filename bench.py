@@ -71,8 +71,8 @@ MEASURED_TRAFFIC = {
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_gemm_w4a4_int4_attn_out_ncu.md"},
     "svdq_gemm_w4a4_int4": {
-        "bytes": 12192256 + 6656,
-        "sources": {"gemm_int4.cu": "1283e16e5c3491e374159d469c4a1f22ec662c02f2db7e3fd7a46b9669f75bcc",
+        "bytes": 12188672 + 1280,
+        "sources": {"gemm_int4.cu": "8d501f172976557d91ca4fba9f9e93abb8197acf27f688ada3365dd8c8d1c426",
                     "device_common.cuh": "aa6078eb6ec5f726d817e11391c6444f445b6172a148942c18c694f17a14beff"},
         "profile": "profiles/svdq_gemm_w4a4_int4_attn_out_ncu.md"},
     "awq_gemv_w4a16": {
@@ -607,7 +607,7 @@ def run_int4(args, lib, dev, stream, world):
     K = N = 3072, rank 32): svdq_quantize_act_int4 and svdq_gemm_w4a4_int4,
     each alone and as the layer's step, weights from svdq_pack_weights_int4
     (three input, weight and output sets rotated, > L2 in all).  The GEMM's
-    denominator is the rate of the warp-level e4m3 MMA it runs on, measured
+    denominator is the rate of the warp-level f16 MMA it runs on, measured
     here (svdq_bench_mma_rate mode 7); the quantizer's is the HBM copy rate."""
     import torch
     case = workloads.CASES["attn_out"]
@@ -656,7 +656,7 @@ def run_int4(args, lib, dev, stream, world):
     t_g = _time_graph(args, launch, gemm, stream, dev, world)
     if int(status.item()) != 0:
         raise RuntimeError("device status set during the INT4 phase")
-    # the e4m3 warp-MMA rate: 128 m16n8k32 MMAs per CTA and iteration, 8 warps
+    # the f16 warp-MMA rate: 128 m16n8k16 MMAs per CTA and iteration, 8 warps
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     iters = 4096
     for _ in range(2):
@@ -666,7 +666,7 @@ def run_int4(args, lib, dev, stream, world):
     lib.bench_mma_rate(7, 128, iters, sms, dev_status=status, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    warp_mma_tflops = 2.0 * 128 * 128 * 32 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    warp_mma_tflops = 2.0 * 128 * 128 * 16 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
     flop = 2.0 * M * N * K
     q_bytes = M * K * 2 + M * K // 2 + M * (K // 64) * 2 + M * r * 2
     gemm_tflops = world * flop / t_g / 1e12
@@ -682,7 +682,7 @@ def run_int4(args, lib, dev, stream, world):
         "quantize_act_int4_traffic": measured_traffic("svdq_quantize_act_int4"),
         "us_gemm_int4": round(t_g * 1e6, 2), "tflops_gemm_int4": round(gemm_tflops, 1),
         "gemm_int4_traffic": measured_traffic("svdq_gemm_w4a4_int4"),
-        "measured_warp_e4m3_mma_tflops": round(warp_mma_tflops, 1),
+        "measured_warp_f16_mma_tflops": round(warp_mma_tflops, 1),
         "gemm_int4_frac_of_warp_mma": round(gemm_tflops / warp_mma_tflops, 4),
     }
 

@@ -8,8 +8,8 @@
 //
 // groups g of 64 consecutive k, codes signed 4-bit integers, scales bf16.
 // B300's tensor cores have no integer 4-bit path (and a slow 8-bit one), so
-// this variant runs on the warp-level FP8 MMA: every code -8..7 is exactly an
-// e4m3 value, the m16n8k32 MMAs of one group accumulate its integer sum
+// this variant runs on the warp-level f16 MMA: every code -8..7 is exactly an
+// f16 value, the m16n8k16 MMAs of one group accumulate its integer sum
 // exactly in fp32 (|sum| <= 64 * 64), and the group's sum is added to the
 // accumulator with one fma by the product sx * sw (exact: two 8-bit
 // significands).  The low-rank up projection runs as bf16 m16n8k16 MMAs into
@@ -18,9 +18,9 @@
 // CTA tile 128 x 128, 16 warps of 32 x 32 (four per scheduler, at most 128
 // registers each); k tiles of 128 (two groups) stream through a 3-stage
 // cp.async ring (codes 64 bytes per row, scales 4 bytes per row).  Each k
-// tile's codes are converted once per CTA into e4m3 tiles (rows of 128
-// bytes, 16-byte pieces XOR-ed by row % 8, read with ldmatrix) by byte-table
-// lookups (prmt), keeping the k order.
+// tile's codes are converted once per CTA into f16 tiles (rows of 256 bytes,
+// the 16-byte pieces of each 128-byte half XOR-ed by row % 8, read with
+// ldmatrix), keeping the k order.
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -39,9 +39,10 @@ constexpr int kStageB = kStageA + kBM * kNibBytes;    // [128][64] codes
 constexpr int kStageSA = kStageB + kBN * kNibBytes;   // [128][2] bf16 scales
 constexpr int kStageSB = kStageSA + kBM * 4;          // [128][2] bf16 scales
 constexpr int kStageBytes = kStageSB + kBN * 4;
-constexpr int kE4A = kStages * kStageBytes;           // [128][128] e4m3
-constexpr int kE4B = kE4A + kBM * kBK;
-constexpr int kSmemBytes = kE4B + kBN * kBK;
+constexpr int kF16Row = kBK * 2;                      // bytes of a converted row
+constexpr int kE4A = kStages * kStageBytes;           // [128][128] f16
+constexpr int kE4B = kE4A + kBM * kF16Row;
+constexpr int kSmemBytes = kE4B + kBN * kF16Row;
 static_assert(kStageBytes % 16 == 0 && kE4A % 128 == 0, "alignment");
 
 SVDQ_DEVINL uint32_t lds32(const uint8_t* p) {
@@ -54,8 +55,9 @@ SVDQ_DEVINL uint32_t lds16(const uint8_t* p) {
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
   return v;
 }
-SVDQ_DEVINL void sts64(uint8_t* p, uint32_t a, uint32_t b) {
-  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(p)), "r"(a), "r"(b)
+SVDQ_DEVINL void sts128v(uint8_t* p, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 SVDQ_DEVINL void ldsm_x4(const uint8_t* p, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -64,37 +66,41 @@ SVDQ_DEVINL void ldsm_x4(const uint8_t* p, uint32_t& r0, uint32_t& r1, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(smem_u32(p)));
 }
-// D[16x8] += A[16x32] B[32x8], e4m3 inputs, fp32 accumulate
-SVDQ_DEVINL void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                uint32_t b1) {
+// D[16x8] += A[16x16] B[16x8], f16 inputs, fp32 accumulate
+SVDQ_DEVINL void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                               uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
       "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// eight two's-complement nibbles (element i at bits 4i..4i+3) -> the e4m3
-// bytes of the same integers, element i in byte i of the pair.  Two 8-entry
-// byte tables indexed by the low three bits (prmt), one for v >= 0
-// (e4m3 of 0..7), one for v < 0 (e4m3 of -8..-1), picked per byte by the
-// nibble's sign bit: the sign bits sit in byte msbs of w (odd elements) and of
-// w << 4 (even elements), and prmt's sign-replicate selectors spread them to
-// whole-byte masks.
 SVDQ_DEVINL uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-SVDQ_DEVINL uint2 nib8_to_e4m3(uint32_t w) {
-  constexpr uint32_t kPosLo = 0x44403800u, kPosHi = 0x4E4C4A48u;  // 3 2 1 0 | 7 6 5 4
-  constexpr uint32_t kNegLo = 0xCACCCED0u, kNegHi = 0xB8C0C4C8u;  // -5 -6 -7 -8 | -1 -2 -3 -4
-  const uint32_t w4 = w << 4;
-  const uint32_t ilo = w & 0x7777u, ihi = (w >> 16) & 0x7777u;
-  const uint32_t mlo = prmt(w4, w, 0xD9C8u), mhi = prmt(w4, w, 0xFBEAu);
-  const uint32_t plo = prmt(kPosLo, kPosHi, ilo), nlo = prmt(kNegLo, kNegHi, ilo);
-  const uint32_t phi = prmt(kPosLo, kPosHi, ihi), nhi = prmt(kNegLo, kNegHi, ihi);
-  return make_uint2((plo & ~mlo) | (nlo & mlo), (phi & ~mhi) | (nhi & mhi));
+SVDQ_DEVINL uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
+// eight two's-complement nibbles (element i at bits 4i..4i+3) -> eight f16
+// values of the same integers, element i in half i of the 16 bytes: v + 8 is
+// the nibble with its top bit flipped; the f16 with bits 0x6400 | (v + 8) is
+// 1024 + v + 8, and subtracting 1032 leaves v exactly
+SVDQ_DEVINL uint4 nib8_to_f16(uint32_t w) {
+  const uint32_t u = w ^ 0x88888888u;
+  const uint32_t t0 = u & 0x0F0F0F0Fu;         // v0, v2, v4, v6 (+ 8), one per byte
+  const uint32_t t1 = (u >> 4) & 0x0F0F0F0Fu;  // v1, v3, v5, v7 (+ 8)
+  const uint32_t lo = prmt(t0, t1, 0x5140u);   // v0, v1, v2, v3
+  const uint32_t hi = prmt(t0, t1, 0x7362u);   // v4, v5, v6, v7
+  constexpr uint32_t kHigh = 0x64646464u, kOff = 0x64086408u;  // f16 1032 twice
+  return make_uint4(hsub2(prmt(lo, kHigh, 0x4140u), kOff), hsub2(prmt(lo, kHigh, 0x4342u), kOff),
+                    hsub2(prmt(hi, kHigh, 0x4140u), kOff), hsub2(prmt(hi, kHigh, 0x4342u), kOff));
+}
+// byte offset of 16-byte piece c (0..15) of row r in a converted tile
+SVDQ_DEVINL int f16_piece(int r, int c) { return r * kF16Row + (((c & 8) | ((c ^ r) & 7)) << 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_int4(const uint8_t* __restrict__ a_codes, const uint16_t* __restrict__ a_scales,
@@ -147,24 +153,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[i][j][c] = 0.0f;
 
-  uint8_t* e4a = smem + kE4A;
-  uint8_t* e4b = smem + kE4B;
+  uint8_t* e4a = smem + kE4A;  // converted A tile (f16)
+  uint8_t* e4b = smem + kE4B;  // converted B tile (f16)
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) load(s);
   for (int kt = 0; kt < KT; ++kt) {
     cp_async_wait<kStages - 2>();  // this thread's copies of tile kt landed
-    __syncthreads();  // ... and every thread's; every warp is done with the e4m3 tiles
+    __syncthreads();  // ... and every thread's; every warp is done with the f16 tiles
     const uint8_t* st = smem + (kt % kStages) * kStageBytes;
-    // codes -> e4m3 tiles: 2 x 128 rows x 16 words of 8 codes
+    // codes -> f16 tiles: 2 x 128 rows x 16 words of 8 codes (one 16-byte
+    // piece each)
 #pragma unroll 2
     for (int i = 0; i < 8; ++i) {
       const int idx = tid + kThreads * i;        // 0 .. 4095
       const int half = idx >> 11, q = idx & 2047;  // A or B; word q of the tile
       const int r = q >> 4, wd = q & 15;
       const uint32_t w = lds32(st + (half ? kStageB : kStageA) + r * kNibBytes + wd * 4);
-      const uint2 e = nib8_to_e4m3(w);
-      sts64((half ? e4b : e4a) + r * kBK + ((((wd >> 1) ^ (r & 7)) << 4) | ((wd & 1) << 3)),
-            e.x, e.y);
+      sts128v((half ? e4b : e4a) + f16_piece(r, wd), nib8_to_f16(w));
     }
     __syncthreads();
     load(kt + kStages - 1);  // into the stage of tile kt - 1, converted last iteration
@@ -179,26 +184,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) part[i][j][c] = 0.0f;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int c0 = h * 4 + kk * 2;  // first 16-byte piece of this k32 step
+      for (int kk = 0; kk < 4; ++kk) {
+        const int c0 = h * 8 + kk * 2;  // first 16-byte piece of this k16 step
         uint32_t a[2][4], b[4][2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int r = wm * 32 + 16 * i + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int c = c0 + (lane >> 4);
-          ldsm_x4(e4a + r * kBK + ((c ^ (r & 7)) << 4), a[i][0], a[i][1], a[i][2], a[i][3]);
+          ldsm_x4(e4a + f16_piece(r, c0 + (lane >> 4)), a[i][0], a[i][1], a[i][2], a[i][3]);
         }
 #pragma unroll
         for (int jp = 0; jp < 2; ++jp) {
           const int r = wn * 32 + 16 * jp + (lane & 7) + (lane >> 4) * 8;
-          const int c = c0 + ((lane >> 3) & 1);
-          ldsm_x4(e4b + r * kBK + ((c ^ (r & 7)) << 4), b[2 * jp][0], b[2 * jp][1],
+          ldsm_x4(e4b + f16_piece(r, c0 + ((lane >> 3) & 1)), b[2 * jp][0], b[2 * jp][1],
                   b[2 * jp + 1][0], b[2 * jp + 1][1]);
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) mma_e4m3_16832(part[i][j], a[i], b[j][0], b[j][1]);
+          for (int j = 0; j < 4; ++j) mma_f16_16816(part[i][j], a[i], b[j][0], b[j][1]);
       }
       // acc += part * (sx sw): the scale product is exact, one rounding per fma
       float2 sw[4];

@@ -13,10 +13,9 @@
 // mode 5: mode 0 with consecutive MMAs alternating between two accumulators
 //         (n = 128: columns 0 and 128)
 // mode 6: mode 3 with the same alternation (n = 128)
-// mode 7: the legacy warp-level MMA of the INT4 variant's GEMM, mma.sync
-//         m16n8k32 e4m3 with fp32 accumulation (n = 128): 8 warps per CTA,
-//         each issuing 16 independent MMAs per iteration, operands in
-//         registers
+// mode 7: the warp-level MMA of the INT4 variant's GEMM, mma.sync m16n8k16
+//         f16 with fp32 accumulation (n = 128): 8 warps per CTA, each issuing
+//         16 independent MMAs per iteration, operands in registers
 #include <cstdint>
 
 #include "../../include/svdq_bench.h"
@@ -145,14 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// mode 7: 8 warps x 16 accumulators; 128 m16n8k32 MMAs per CTA and iteration
-// (2 * 16 * 8 * 32 * 128 = 2 * 128 * 128 * 32 flops, the formula with n = 128,
-// K_mma = 32).  Operands: e4m3 1.0 (0x38) and 2.0 (0x40).  The accumulators
+// mode 7: 8 warps x 16 accumulators; 128 m16n8k16 MMAs per CTA and iteration
+// (2 * 16 * 8 * 16 * 128 = 2 * 128 * 128 * 16 flops, the formula with n = 128,
+// K_mma = 16).  Operands: f16 1.0 (0x3C00) and 2.0 (0x4000).  The accumulators
 // feed a store under a condition the compiler cannot decide (iters < 0; the
 // host rejects it), so that no MMA is dead code.
 __global__ void __launch_bounds__(256, 1) k_mma_rate_warp(int iters, int* dev_status) {
-  const uint32_t a0 = 0x38403840u, a1 = 0x40383840u, a2 = 0x38384040u, a3 = 0x40404038u,
-                 b0 = 0x38383838u, b1 = 0x40384038u;
+  const uint32_t a0 = 0x3C004000u, a1 = 0x40003C00u, a2 = 0x3C003C00u, a3 = 0x40004000u,
+                 b0 = 0x3C003C00u, b1 = 0x40003C00u;
   float d[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j)
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(256, 1) k_mma_rate_warp(int iters, int* dev_st
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       asm volatile(
-          "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, "
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
           "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
           : "+f"(d[j][0]), "+f"(d[j][1]), "+f"(d[j][2]), "+f"(d[j][3])
           : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

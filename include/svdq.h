@@ -382,8 +382,8 @@ svdq_status svdq_quantize_act_int4(const uint16_t* X_bf16, const float* inv_lamb
  *                   + sum_i lora_act[m][i] L2[n][i] + bias[n] )
  * fp32 accumulation: each group's integer sum is exact, then added with one
  * fma by the (exact) product of its two scales; one rounding to bf16.  B300
- * has no 4-bit integer tensor-core path: the codes run on the warp-level FP8
- * MMA (every code is an exact e4m3 value).
+ * has no 4-bit integer tensor-core path: the codes run on the warp-level f16
+ * MMA (every code is an exact f16 value).
  * Inputs: a_codes [M][K/2], a_scales [M][K/64] bf16 (svdq_quantize_act_int4),
  * w_codes [N][K/2], w_scales [N][K/64] bf16, L2 [N][rank] bf16
  * (svdq_pack_weights_int4), lora_act [M][rank] bf16, bias [N] bf16 or NULL.
