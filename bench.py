@@ -606,9 +606,9 @@ def run_int4(args, lib, dev, stream, world):
     """The INT4 variant at the attention out-projection shape (M = 4096,
     K = N = 3072, rank 32): svdq_quantize_act_int4 and svdq_gemm_w4a4_int4,
     each alone and as the layer's step, weights from svdq_pack_weights_int4
-    (three input, weight and output sets rotated, > L2 in all).  The GEMM's
-    denominator is the rate of the warp-level f16 MMA it runs on, measured
-    here (svdq_bench_mma_rate mode 7); the quantizer's is the HBM copy rate."""
+    (three input, weight and output sets rotated, > L2 in all).  The GEMM runs
+    on tcgen05 f16 MMAs: its denominator is the measured bf16 tensor rate (the
+    f16 rate of the same instruction); the quantizer's is the HBM copy rate."""
     import torch
     case = workloads.CASES["attn_out"]
     M, K, N, r = case.M, case.K, case.N, case.rank
@@ -642,7 +642,7 @@ def run_int4(args, lib, dev, stream, world):
 
     def gemm(s, st):
         lib.svdq_gemm_w4a4_int4(s["ac"], s["as"], s["wc"], s["ws"], s["lora"], s["L2"],
-                                s["bias"], M, N, K, r, s["Y"], stream=st)
+                                s["bias"], M, N, K, r, s["Y"], dev_status=status, stream=st)
 
     def step(s, st):
         quant(s, st)
@@ -656,21 +656,11 @@ def run_int4(args, lib, dev, stream, world):
     t_g = _time_graph(args, launch, gemm, stream, dev, world)
     if int(status.item()) != 0:
         raise RuntimeError("device status set during the INT4 phase")
-    # the f16 warp-MMA rate: 128 m16n8k16 MMAs per CTA and iteration, 8 warps
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    iters = 4096
-    for _ in range(2):
-        lib.bench_mma_rate(7, 128, iters, sms, dev_status=status, stream=stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    lib.bench_mma_rate(7, 128, iters, sms, dev_status=status, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    warp_mma_tflops = 2.0 * 128 * 128 * 16 * iters * sms / (e0.elapsed_time(e1) * 1e-3) / 1e12
     flop = 2.0 * M * N * K
     q_bytes = M * K * 2 + M * K // 2 + M * (K // 64) * 2 + M * r * 2
     gemm_tflops = world * flop / t_g / 1e12
-    hbm = peaks()["hbm_gbs"]
+    pk = peaks()
+    hbm = pk["hbm_gbs"]
     return {
         "workload": f"attn_out, INT4 variant: M={M} K={K} N={N} rank={r}, group 64, bf16 "
                     f"scales", "launches": 4 * args.steps,
@@ -682,8 +672,9 @@ def run_int4(args, lib, dev, stream, world):
         "quantize_act_int4_traffic": measured_traffic("svdq_quantize_act_int4"),
         "us_gemm_int4": round(t_g * 1e6, 2), "tflops_gemm_int4": round(gemm_tflops, 1),
         "gemm_int4_traffic": measured_traffic("svdq_gemm_w4a4_int4"),
-        "measured_warp_f16_mma_tflops": round(warp_mma_tflops, 1),
-        "gemm_int4_frac_of_warp_mma": round(gemm_tflops / warp_mma_tflops, 4),
+        "gemm_int4_peak_tflops": pk["bf16_tflops"],
+        "gemm_int4_frac": round(gemm_tflops / pk["bf16_tflops"], 4),
+        "gemm_int4_peak_source": f"{pk['source']} bf16 (tcgen05 f16 and bf16 MMAs run at one rate)",
     }
 
 

@@ -47,7 +47,7 @@ _SIGS = {
     "svdq_quantize_act_int4": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p,
                                       _c_p, _c_p]),
     "svdq_gemm_w4a4_int4": (_i32, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32,
-                                   _i32, _i32, _c_p]),
+                                   _i32, _i32, _c_p, _c_p]),
     "svdq_quantize_act": (_i32, [_c_p, _c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p,
                                  _c_p]),
     "svdq_gemm_w4a4": (_i32, [_c_p, _c_p, _c_p, _c_p, _f32, _c_p, _c_p, _c_p, _c_p, _i32,
@@ -291,13 +291,13 @@ def svdq_quantize_act_int4(X, inv_lambda, L1s, rank: int, a_codes=None, a_scales
 
 
 def svdq_gemm_w4a4_int4(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias, M: int,
-                        N: int, K: int, rank: int, Y=None, stream=None):
+                        N: int, K: int, rank: int, Y=None, dev_status=None, stream=None):
     """INT4 variant.  a_scales [M, K/64] and w_scales [N, K/64] bf16, L2
     [N, rank] bf16.  Returns Y [M, N] bf16 (CUDA)."""
     torch = _torch()
     for t, n in ((a_codes, "a_codes"), (a_scales, "a_scales"), (w_codes, "w_codes"),
                  (w_scales, "w_scales"), (lora_act, "lora_act"), (L2, "L2"), (bias, "bias"),
-                 (Y, "Y")):
+                 (Y, "Y"), (dev_status, "dev_status")):
         _check_cuda(t, n)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=a_codes.device)
@@ -307,12 +307,13 @@ def svdq_gemm_w4a4_int4(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias
                            (w_codes, "w_codes", code_bytes(N, K), 1),
                            (w_scales, "w_scales", N * (K // 64), 2),
                            (lora_act, "lora_act", M * rank, 2), (L2, "L2", N * rank, 2),
-                           (bias, "bias", N, 2), (Y, "Y", M * N, 2)):
+                           (bias, "bias", N, 2), (Y, "Y", M * N, 2),
+                           (dev_status, "dev_status", 1, 4)):
             _need(t, n, e, z)
     st = _lib.svdq_gemm_w4a4_int4(_dptr(a_codes), _dptr(a_scales), _dptr(w_codes),
                                   _dptr(w_scales), _dptr(lora_act), _dptr(L2), _dptr(bias),
                                   _dptr(Y), int(M), int(N), int(K), int(rank),
-                                  _stream_ptr(stream))
+                                  _dptr(dev_status), _stream_ptr(stream))
     _check(st, "svdq_gemm_w4a4_int4")
     return Y
 

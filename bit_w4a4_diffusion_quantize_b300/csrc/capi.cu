@@ -328,7 +328,7 @@ svdq_status svdq_gemm_w4a4_int4(const uint8_t* a_codes, const uint16_t* a_scales
                                 const uint8_t* w_codes, const uint16_t* w_scales,
                                 const uint16_t* lora_act, const uint16_t* L2,
                                 const uint16_t* bias, uint16_t* Y, int M, int N, int K, int rank,
-                                void* stream) {
+                                int* dev_status, void* stream) {
   if (M < 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0) return SVDQ_ERR_SHAPE;
   if (!rank_ok(rank)) return SVDQ_ERR_RANK;
   if (M == 0) return SVDQ_OK;
@@ -341,7 +341,8 @@ svdq_status svdq_gemm_w4a4_int4(const uint8_t* a_codes, const uint16_t* a_scales
   svdq_status st = current_device(nullptr, nullptr);
   if (st != SVDQ_OK) return st;
   cudaError_t e = svdq::launch_gemm_int4(a_codes, a_scales, w_codes, w_scales, lora_act, L2, bias,
-                                         Y, M, N, K, rank, static_cast<cudaStream_t>(stream));
+                                         Y, M, N, K, rank, dev_status,
+                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVDQ_OK : SVDQ_ERR_CUDA;
 }
 

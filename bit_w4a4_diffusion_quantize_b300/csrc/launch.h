@@ -19,7 +19,8 @@ cudaError_t launch_quantize_act(const CUtensorMap& tm_x, const CUtensorMap& tm_l
 cudaError_t launch_gemm_int4(const uint8_t* a_codes, const uint16_t* a_scales,
                              const uint8_t* w_codes, const uint16_t* w_scales,
                              const uint16_t* lora_act, const uint16_t* L2, const uint16_t* bias,
-                             uint16_t* Y, int M, int N, int K, int rank, cudaStream_t stream);
+                             uint16_t* Y, int M, int N, int K, int rank, int* dev_status,
+                             cudaStream_t stream);
 
 // Tensor maps of svdq_gemm_w4a4 (and of its GELU and QKV variants).  The
 // kernel runs on CTA pairs: each CTA loads its own 128 A rows and one half

@@ -13,9 +13,9 @@
 // mode 5: mode 0 with consecutive MMAs alternating between two accumulators
 //         (n = 128: columns 0 and 128)
 // mode 6: mode 3 with the same alternation (n = 128)
-// mode 7: the warp-level MMA of the INT4 variant's GEMM, mma.sync m16n8k16
-//         f16 with fp32 accumulation (n = 128): 8 warps per CTA, each issuing
-//         16 independent MMAs per iteration, operands in registers
+// mode 7: the legacy warp-level MMA, mma.sync m16n8k16 f16 with fp32
+//         accumulation (n = 128): 8 warps per CTA, each issuing 16
+//         independent MMAs per iteration, operands in registers
 #include <cstdint>
 
 #include "../../include/svdq_bench.h"

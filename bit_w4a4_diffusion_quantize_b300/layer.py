@@ -92,7 +92,7 @@ class SVDQLinearInt4:
             stream=stream)
         return _lib.svdq_gemm_w4a4_int4(a_codes, a_scales, self.w_codes, self.w_scales, lora,
                                         self.L2, self.bias, M, self.N, self.K, self.rank, out,
-                                        stream=stream)
+                                        dev_status=dev_status, stream=stream)
 
     __call__ = forward
 

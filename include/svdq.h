@@ -382,8 +382,10 @@ svdq_status svdq_quantize_act_int4(const uint16_t* X_bf16, const float* inv_lamb
  *                   + sum_i lora_act[m][i] L2[n][i] + bias[n] )
  * fp32 accumulation: each group's integer sum is exact, then added with one
  * fma by the (exact) product of its two scales; one rounding to bf16.  B300
- * has no 4-bit integer tensor-core path: the codes run on the warp-level f16
- * MMA (every code is an exact f16 value).
+ * has no 4-bit integer tensor-core path: every code is an exact f16 value,
+ * and each group's sum comes from tcgen05 f16 MMAs into tensor memory.
+ * dev_status (nullable device int): SVDQ_DEV_TIMEOUT if an internal pipeline
+ * wait exceeded its bound (the output is then incomplete).
  * Inputs: a_codes [M][K/2], a_scales [M][K/64] bf16 (svdq_quantize_act_int4),
  * w_codes [N][K/2], w_scales [N][K/64] bf16, L2 [N][rank] bf16
  * (svdq_pack_weights_int4), lora_act [M][rank] bf16, bias [N] bf16 or NULL.
@@ -396,7 +398,7 @@ svdq_status svdq_gemm_w4a4_int4(const uint8_t* a_codes, const uint16_t* a_scales
                                 const uint8_t* w_codes, const uint16_t* w_scales,
                                 const uint16_t* lora_act, const uint16_t* L2,
                                 const uint16_t* bias, uint16_t* Y, int M, int N, int K,
-                                int rank, void* stream);
+                                int rank, int* dev_status, void* stream);
 
 /* AWQ W4A16 GEMV for the small-M modulation layers (kernel-family list:
  * memory-bound adaLN modulation):

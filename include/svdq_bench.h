@@ -19,10 +19,10 @@
  *   mode 5: mode 0 with consecutive MMAs alternating between two
  *           accumulators (n = 128 only)
  *   mode 6: mode 3 with the same alternation (n = 128 only)
- *   mode 7: the warp-level MMA of svdq_gemm_w4a4_int4 (mma.sync m16n8k16,
- *           f16 inputs, fp32 accumulate; operands in registers, 8 warps per
- *           CTA, 16 independent accumulators per warp), K_mma = 16, n = 128
- *           only: 128 such MMAs per CTA and iteration
+ *   mode 7: the legacy warp-level MMA (mma.sync m16n8k16, f16 inputs, fp32
+ *           accumulate; operands in registers, 8 warps per CTA, 16
+ *           independent accumulators per warp), K_mma = 16, n = 128 only:
+ *           128 such MMAs per CTA and iteration
  * For modes 3, 4 and 6 the work is 2 * 256 * n * K_mma * iters * ctas / 2
  * flops, the same total as the formula above.
  *

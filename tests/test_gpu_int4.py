@@ -133,14 +133,16 @@ def test_quantize_act_int4_empty():
 
 # --------------------------------------------------------------------------- GEMM
 def _gemm(out, packed, b, M, N, K, rank, bias=True):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     Y = lib.svdq_gemm_w4a4_int4(
         dev_u8(int4.pack_codes(out["a_codes"])), dev_bits16(int4.scale_bits(out["a_scales"])),
         dev_u8(int4.pack_codes(packed["w_codes"])),
         dev_bits16(int4.scale_bits(packed["w_scales"])),
         dev_bits16(formats.bf16_bits(out["lora_act"])),
         dev_bits16(formats.bf16_bits(packed["L2"]).T.copy()),
-        dev_bf16(b) if bias else None, M, N, K, rank)
+        dev_bf16(b) if bias else None, M, N, K, rank, dev_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status set"
     return host_bf16(Y)
 
 

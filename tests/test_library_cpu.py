@@ -176,7 +176,7 @@ def _qa4(X=ALIGNED, M=64, K=256, r=32, sc=ALIGNED, lora=ALIGNED):
 
 def _g4(M=64, N=256, K=256, r=32, Y=ALIGNED, a=ALIGNED, sw=ALIGNED, bias=None):
     return lib.raw_lib().svdq_gemm_w4a4_int4(a, ALIGNED, ALIGNED, sw, ALIGNED, ALIGNED, bias, Y,
-                                             M, N, K, r, None)
+                                             M, N, K, r, None, None)
 
 
 def test_int4_argument_errors():
